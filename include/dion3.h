@@ -1,0 +1,230 @@
+/*
+ * dion3.h - C ABI of the Dion3 optimizer step on one GB300 (sm_103a).
+ *
+ * The Dion3 step (source: "Dion3: Full-Stack Orthogonal Updates", the agihunt
+ * summary of the paper, paragraphs on the first level - Gram Newton-Schulz -
+ * and the third level - fractional row selection) for one n x m matrix:
+ *
+ *   (a) M <- M + G on every row; S = the k = ceil(f n) rows of M with the
+ *       largest l1 norm (ties to the lower row index), ascending;
+ *   (b) X = M[S] / (||M[S]||_F + eps) in fp16; Gram Newton-Schulz: R = X X^T,
+ *       T iterations of Z = aI + bR + cR^2, Q <- Z Q, R <- Z R Z, a restart
+ *       before iteration `restart_iter` (X <- Q X, R = X X^T, Q <- I), and
+ *       O = Q X at the end (on X^T when k > m: the Gram matrix is formed on the
+ *       short side);
+ *   (c) W[S] <- W[S] - (lr / sqrt(f)) O; M[S] <- mu M[S]; other rows of W and
+ *       M are not touched (error feedback).
+ *
+ * Conventions shared by every entry point:
+ *   - Memory: every tensor and the workspace is caller-owned DEVICE memory; the
+ *     library never allocates device memory.  Arrays of pointers
+ *     (dion3_group.params, ...) are HOST arrays read during the call only.
+ *   - Layout: matrices are dense row-major with row pitch == cols; each device
+ *     pointer must be 16-byte aligned; the workspace 256-byte aligned.
+ *   - Ordering: every call only enqueues work on `stream` and returns without
+ *     synchronising; results are visible to later work on the same stream.
+ *     Calls that share one workspace must not overlap on the device.
+ *   - Errors: arguments are validated on the host before the first launch; an
+ *     invalid call returns a status != DION3_OK, enqueues nothing and leaves
+ *     every tensor untouched.  A failed launch returns DION3_ERR_CUDA.
+ *     dion3_last_error() gives a one-line description (per host thread).
+ *   - Device-side waits in the tensor-core kernels are bounded (about one
+ *     second); a wait that runs out records DION3_ERR_TIMEOUT in a device
+ *     status word that dion3_device_status() reads.
+ *   - Exceptions never cross this boundary.
+ */
+#ifndef DION3_H_
+#define DION3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DION3_ABI_VERSION 1
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* dion3_stream_t;
+
+typedef enum {
+  DION3_OK = 0,
+  DION3_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad hyperparameter, misalignment */
+  DION3_ERR_UNSUPPORTED = 2,  /* valid request that this build does not implement */
+  DION3_ERR_WORKSPACE = 3,    /* workspace null or smaller than the *_workspace_size query */
+  DION3_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  DION3_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out (see dion3_device_status) */
+  DION3_ERR_DEVICE_CHECK = 6  /* a device-side consistency check failed */
+} dion3_status;
+
+typedef enum { DION3_F32 = 0, DION3_BF16 = 1, DION3_F16 = 2 } dion3_dtype;
+
+/*
+ * Hyperparameters of one step.
+ *   f            fraction of rows orthogonalised, 0 < f <= 1; k = ceil(f n)
+ *                (third-level paragraph of the summary page).
+ *   mu           decay of the selected momentum rows (error feedback).
+ *   lr           base learning rate; the applied rate is lr / sqrt(f), computed
+ *                in double on the host and passed to the kernels as fp32.
+ *   eps          X / (||X||_F + eps) before Newton-Schulz.
+ *   ns_steps     T >= 1 Newton-Schulz iterations.
+ *   restart_iter 0 for no restart, else 2..T: the 1-based iteration the
+ *                restart comes before (the pages restart at iteration 3).
+ *   a, b, c      the polynomial Z = aI + bR + cR^2.
+ *   ns_dtype     arithmetic type of Gram-NS operands: DION3_F16 (fp32
+ *                accumulation).  Other values return DION3_ERR_UNSUPPORTED.
+ */
+typedef struct {
+  float f;
+  float mu;
+  float lr;
+  float eps;
+  int32_t ns_steps;
+  int32_t restart_iter;
+  float a, b, c;
+  int32_t ns_dtype;
+} dion3_hparams;
+
+/*
+ * A shape group ("megabatch"): `batch` matrices of the same rows x cols, all
+ * with the same dtypes, stepped by batched launches.
+ *   params      host array [batch] of device pointers to W (param_dtype:
+ *               DION3_F32 or DION3_BF16), updated in place.
+ *   grads       host array [batch] of device pointers to G (grad_dtype:
+ *               DION3_F32 or DION3_BF16), read only.
+ *   momentum    host array [batch] of device pointers to M (fp32), updated in
+ *               place.
+ */
+typedef struct {
+  int32_t rows;
+  int32_t cols;
+  int32_t batch;
+  int32_t param_dtype;
+  int32_t grad_dtype;
+  void* const* params;
+  const void* const* grads;
+  float* const* momentum;
+} dion3_group;
+
+/* DION3_ABI_VERSION of the loaded library. */
+size_t dion3_abi_version(void);
+
+/* Static description of a status code (never NULL). */
+const char* dion3_status_string(int status);
+
+/* Description of the last error returned on this host thread ("" if none). */
+const char* dion3_last_error(void);
+
+/* Number of selected rows k = ceil(f * rows), clamped to [1, rows]; 0 if the
+ * arguments are invalid. */
+int32_t dion3_num_selected(float f, int32_t rows);
+
+/*
+ * Useful FLOPs of the Gram-NS schedule this library runs on one k x m
+ * submatrix with `hp` (a triangle counted as half): with s = min(k, m),
+ * L = max(k, m), one SYRK costs s^2 L, a symmetric s^3 product s^3 and a
+ * rectangular multiply 2 s^2 L.  T = 5 with a restart gives 6 s^2 L + 14 s^3.
+ * Returns a negative value for invalid arguments.
+ */
+double dion3_useful_flops(int32_t k, int32_t m, const dion3_hparams* hp);
+
+/*
+ * Workspace bytes needed by dion3_select_rows for `batch` matrices of
+ * rows x cols and k selected rows.
+ */
+dion3_status dion3_select_workspace_size(int32_t rows, int32_t cols, int32_t batch,
+                                         int32_t k, size_t* bytes);
+
+/*
+ * Step (a) alone: optional accumulation and l1 top-k selection.
+ *   momentum  host array [batch] of device pointers to fp32 rows x cols M.
+ *   grads     host array [batch] of device pointers to G (grad_dtype), or NULL:
+ *             with grads, M <- M + G (fp32, round-to-nearest, every row) first;
+ *             with NULL, M is only read.
+ *   k         1 <= k <= rows rows selected per matrix.
+ *   idx_out   device int32 [batch][k]: selected row indices, ascending.
+ *   fro2_out  device fp32 [batch]: sum of squares of the selected rows of M
+ *             (||M[S]||_F^2), or NULL.
+ * Ties in l1 go to the lower row index.
+ */
+dion3_status dion3_select_rows(int32_t rows, int32_t cols, int32_t batch,
+                               float* const* momentum, const void* const* grads,
+                               int32_t grad_dtype, int32_t k, int32_t* idx_out,
+                               float* fro2_out, void* ws, size_t ws_bytes,
+                               dion3_stream_t stream);
+
+/* Workspace bytes needed by dion3_gram_ns_batched. */
+dion3_status dion3_gram_ns_workspace_size(int32_t k, int32_t m, int32_t batch,
+                                          const dion3_hparams* hp, size_t* bytes);
+
+/*
+ * Step (b) alone: Gram Newton-Schulz of `batch` fp16 k x m matrices.
+ *   X  device fp16 [batch][k][m], read only.
+ *   O  device fp16 [batch][k][m]: O = GramNS(X / (||X||_F + hp->eps)).
+ * Only hp->eps, ns_steps, restart_iter, a, b, c and ns_dtype are used.
+ * Operands are fp16 with fp32 accumulation; R, Z, Q and the products are
+ * rounded to fp16 between steps (first-level paragraph: the method runs in
+ * float16).
+ */
+dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const void* X,
+                                   void* O, const dion3_hparams* hp, void* ws,
+                                   size_t ws_bytes, dion3_stream_t stream);
+
+typedef enum { DION3_GEMM_RECT = 0, DION3_GEMM_SYM_LOWER = 1 } dion3_gemm_mode;
+
+/*
+ * The tensor-core GEMM behind step (b), callable on its own.  Second-level
+ * paragraph of the summary page: a symmetric product needs only its lower
+ * triangle, which is then copied to the upper one.  Computes
+ *     V = alpha A B^T + beta C + gamma I,  rounded to fp16 (fp32 accumulation),
+ * with A [batch][M][K] and B [batch][N][K] fp16 (K contiguous, pitches lda /
+ * ldb elements, batch strides in elements) and C [batch][M][N] fp16 or NULL
+ * (then beta is ignored).
+ *   DION3_GEMM_RECT:      every 128 x 128 output tile; V goes to D [batch][M][N]
+ *                         (pitch ldd) if D is not NULL, and V^T to DT
+ *                         [batch][N][M] (pitch lddt) if DT is not NULL; at least
+ *                         one of them.
+ *   DION3_GEMM_SYM_LOWER: M == N; only lower-triangle tiles are computed, each
+ *                         written in place and mirrored, so D is exactly
+ *                         symmetric (DT must be NULL).  Correct whenever
+ *                         A B^T is symmetric: A == B, or A and B commuting
+ *                         symmetric matrices (then B^T = B).
+ * Rules: A and B 16-byte aligned; lda, ldb >= K and multiples of 8; their batch
+ * strides multiples of 8.  D, DT and C may have any pitch >= their row length.
+ */
+dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t batch,
+                            const void* A, int32_t lda, int64_t a_bstride,
+                            const void* B, int32_t ldb, int64_t b_bstride,
+                            const void* C, int32_t ldc, int64_t c_bstride,
+                            void* D, int32_t ldd, int64_t d_bstride,
+                            void* DT, int32_t lddt, int64_t dt_bstride,
+                            float alpha, float beta, float gamma, dion3_stream_t stream);
+
+/* Workspace bytes needed by dion3_step for these groups. */
+dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups,
+                                  const dion3_hparams* hp, size_t* bytes);
+
+/*
+ * The whole Dion3 step (a)-(c) over `ngroups` shape groups.
+ *   sel_idx_out  NULL, or a host array [ngroups] of device int32 [batch][k]
+ *                buffers (entries may be NULL) that receive each matrix's
+ *                selected rows, ascending.
+ * Groups are processed in order on `stream`.
+ */
+dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
+                        const dion3_hparams* hp, void* ws, size_t ws_bytes,
+                        int32_t* const* sel_idx_out, dion3_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word written by
+ * bounded device-side waits, and returns DION3_OK, DION3_ERR_TIMEOUT or
+ * DION3_ERR_DEVICE_CHECK (or DION3_ERR_CUDA if synchronisation fails).
+ */
+dion3_status dion3_device_status(dion3_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* DION3_H_ */

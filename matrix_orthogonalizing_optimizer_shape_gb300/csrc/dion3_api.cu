@@ -1,0 +1,610 @@
+// C ABI of the Dion3 step (include/dion3.h): argument validation, workspace
+// planning, and the launch schedule of steps (a)-(c) on one stream.
+//
+// Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of the
+// paper): first-level paragraph (Gram Newton-Schulz with a restart at
+// iteration 3, float16) and third-level paragraph (l1 selection of
+// k = ceil(f n) rows, update of those rows only, lr ~ 1/sqrt(f), decay of the
+// selected momentum rows by mu).  Megabatching (fourth-level paragraph) becomes
+// shape-grouped batched launches on one GPU.
+#include "../../include/dion3.h"
+#include "internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdlib>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+namespace dion3 {
+
+__device__ unsigned g_device_status = 0u;
+
+unsigned* device_status_ptr() {
+  static std::mutex mu;
+  static std::vector<unsigned*> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, nullptr);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+thread_local std::string t_last_error;
+
+dion3_status fail(dion3_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+dion3_status fail(dion3_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+dion3_status ok() {
+  t_last_error.clear();
+  return DION3_OK;
+}
+
+inline long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dion3_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DION3_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Host-side fault injection for tests of error propagation: DION3_INJECT=
+// launch_fail makes the first launch of a call report a CUDA error without
+// launching anything.
+bool inject_launch_fail() {
+  const char* v = getenv("DION3_INJECT");
+  return v != nullptr && strcmp(v, "launch_fail") == 0;
+}
+
+dion3_status check_hparams(const dion3_hparams* hp, bool need_step_fields) {
+  if (hp == nullptr) return fail(DION3_ERR_INVALID_ARG, "hparams is NULL");
+  if (hp->ns_steps < 1 || hp->ns_steps > 64) return fail(DION3_ERR_INVALID_ARG, "ns_steps must lie in [1, 64]");
+  if (hp->restart_iter != 0 && (hp->restart_iter < 2 || hp->restart_iter > hp->ns_steps))
+    return fail(DION3_ERR_INVALID_ARG, "restart_iter must be 0 or lie in [2, ns_steps]");
+  if (!std::isfinite(hp->a) || !std::isfinite(hp->b) || !std::isfinite(hp->c))
+    return fail(DION3_ERR_INVALID_ARG, "NS coefficients must be finite");
+  if (!(hp->eps >= 0.0f) || !std::isfinite(hp->eps)) return fail(DION3_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (hp->ns_dtype != DION3_F16) return fail(DION3_ERR_UNSUPPORTED, "ns_dtype: only DION3_F16 is implemented");
+  if (need_step_fields) {
+    if (!(hp->f > 0.0f && hp->f <= 1.0f)) return fail(DION3_ERR_INVALID_ARG, "f must lie in (0, 1]");
+    if (!std::isfinite(hp->mu)) return fail(DION3_ERR_INVALID_ARG, "mu must be finite");
+    if (!std::isfinite(hp->lr)) return fail(DION3_ERR_INVALID_ARG, "lr must be finite");
+  }
+  return DION3_OK;
+}
+
+int32_t num_selected(float f, int32_t rows) {
+  if (!(f > 0.0f && f <= 1.0f) || rows < 1) return 0;
+  const double k = std::ceil(static_cast<double>(f) * static_cast<double>(rows));
+  if (k < 1.0) return 1;
+  if (k > rows) return rows;
+  return static_cast<int32_t>(k);
+}
+
+// ---------------------------------------------------------------------------
+// Workspace planning
+// ---------------------------------------------------------------------------
+struct Carver {
+  char* base;  // may be null (size query)
+  size_t off = 0;
+  template <class T>
+  T* take(long long count) {
+    off = static_cast<size_t>(round_up(static_cast<long long>(off), 256));
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += static_cast<size_t>(count) * sizeof(T);
+    return p;
+  }
+};
+
+// Gram-NS buffers for `batch` k x m problems.  Y is the s x L operand (s =
+// min(k, m)); Yt0/Yt1 hold L x s transposes; S[0..3] are s x s buffers.
+struct NsPlan {
+  int k, m, batch, s, L, sp, Lp;
+  bool wide;  // k <= m: Y = X; else Y = X^T
+  __half* Y;
+  __half* Yt[2];
+  __half* S[4];
+  long long y_bs, yt_bs, s_bs;
+};
+
+void plan_ns(Carver& c, int k, int m, int batch, NsPlan& p) {
+  p.k = k;
+  p.m = m;
+  p.batch = batch;
+  p.wide = k <= m;
+  p.s = p.wide ? k : m;
+  p.L = p.wide ? m : k;
+  p.sp = static_cast<int>(round_up(p.s, 8));
+  p.Lp = static_cast<int>(round_up(p.L, 8));
+  p.y_bs = static_cast<long long>(p.s) * p.Lp;
+  p.yt_bs = static_cast<long long>(p.L) * p.sp;
+  p.s_bs = static_cast<long long>(p.s) * p.sp;
+  p.Y = c.take<__half>(p.y_bs * batch);
+  p.Yt[0] = c.take<__half>(p.yt_bs * batch);
+  p.Yt[1] = c.take<__half>(p.yt_bs * batch);
+  for (int i = 0; i < 4; ++i) p.S[i] = c.take<__half>(p.s_bs * batch);
+}
+
+// Where the gather kernel writes the two orientations of the normalised rows.
+void gather_targets(const NsPlan& p, GatherArgs& g) {
+  // Rows orientation: k x m, pitch round_up(m, 8); columns: m x k, pitch
+  // round_up(k, 8).
+  if (p.wide) {
+    g.out_rows = p.Y;      g.rows_bstride = p.y_bs;  g.ld_rows = p.Lp;
+    g.out_cols = p.Yt[0];  g.cols_bstride = p.yt_bs; g.ld_cols = p.sp;
+  } else {
+    g.out_rows = p.Yt[0];  g.rows_bstride = p.yt_bs; g.ld_rows = p.sp;
+    g.out_cols = p.Y;      g.cols_bstride = p.y_bs;  g.ld_cols = p.Lp;
+  }
+}
+
+// Useful FLOPs of the schedule run_gram_ns() launches (triangle = half).
+double schedule_flops(int k, int m, const dion3_hparams& hp) {
+  const double s = std::min(k, m), L = std::max(k, m);
+  const double syrk = s * s * L, sym = s * s * s, rect = 2.0 * s * s * L;
+  double f = syrk;
+  bool q_identity = true;
+  const int T = hp.ns_steps, rs = hp.restart_iter;
+  for (int t = 1; t <= T; ++t) {
+    if (rs > 1 && t == rs) {
+      f += rect + syrk;
+      q_identity = true;
+    }
+    f += sym;  // Z
+    if (!q_identity) f += sym;
+    q_identity = false;
+    if (t < T && t + 1 != rs) f += 2.0 * sym;
+  }
+  return f + rect;
+}
+
+// ---------------------------------------------------------------------------
+// Gram Newton-Schulz schedule (first-level paragraph of the summary page):
+//   R = Y Y^T;  for t = 1..T:
+//     [t == restart] Y <- Q Y (written as Y^T Q and its transpose), R = Y Y^T, Q <- I
+//     Z = aI + bR + cR^2;  Q <- Z (Q = I) or Q <- Z Q;
+//     [t < T and t + 1 != restart] R <- Z (R Z)
+//   O = Q Y  (written in the k x m orientation of X).
+// ---------------------------------------------------------------------------
+struct NsOut {
+  __half* O;
+  long long o_bs;
+  int ld_o;
+};
+
+dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
+                         cudaStream_t stream) {
+  auto sym = [&](const __half* A, const __half* B, __half* D, int K, const __half* C, float alpha, float beta,
+                 float gamma, const __half* Abase_is_Y) -> GemmDesc {
+    GemmDesc g{};
+    const bool from_y = Abase_is_Y != nullptr;
+    g.A = A; g.a_bstride = from_y ? p.y_bs : p.s_bs; g.lda = from_y ? p.Lp : p.sp;
+    g.B = B; g.b_bstride = from_y ? p.y_bs : p.s_bs; g.ldb = from_y ? p.Lp : p.sp;
+    g.M = p.s; g.N = p.s; g.K = K; g.batch = p.batch;
+    g.mode = kSymLower;
+    g.alpha = alpha; g.beta = beta; g.gamma = gamma;
+    g.C = C; g.c_bstride = p.s_bs; g.ldc = p.sp;
+    g.out = D; g.out_bstride = p.s_bs; g.ld_out = p.sp;
+    return g;
+  };
+  auto launch = [&](const GemmDesc& g) -> dion3_status {
+    const char* why = nullptr;
+    if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
+    const cudaError_t e = launch_gemm(g, st, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return DION3_OK;
+  };
+  dion3_status rc;
+
+  // s x s buffer roles: indices into p.S.
+  int R = 0, Z = -1, Q = -1;
+  auto free_buf = [&](int a, int b, int c) {
+    for (int i = 0; i < 4; ++i)
+      if (i != a && i != b && i != c) return i;
+    return -1;
+  };
+  int ycur = 0;  // Yt[ycur] is the current Y^T
+
+  // R = Y Y^T
+  if ((rc = launch(sym(p.Y, p.Y, p.S[R], p.L, nullptr, 1.f, 0.f, 0.f, p.Y))) != DION3_OK) return rc;
+  const int T = hp.ns_steps, rs = hp.restart_iter;
+  for (int t = 1; t <= T; ++t) {
+    if (rs > 1 && t == rs) {
+      // Y <- Q Y:  D = Y^T Q (L x s) is the new Y^T; its transpose the new Y.
+      GemmDesc g{};
+      g.A = p.Yt[ycur]; g.a_bstride = p.yt_bs; g.lda = p.sp;
+      g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
+      g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
+      g.mode = kRect; g.alpha = 1.f;
+      g.out = p.Yt[ycur ^ 1]; g.out_bstride = p.yt_bs; g.ld_out = p.sp;
+      g.outT = p.Y; g.outT_bstride = p.y_bs; g.ld_outT = p.Lp;
+      if ((rc = launch(g)) != DION3_OK) return rc;
+      ycur ^= 1;
+      if ((rc = launch(sym(p.Y, p.Y, p.S[R], p.L, nullptr, 1.f, 0.f, 0.f, p.Y))) != DION3_OK) return rc;
+      Q = -1;
+    }
+    // Z = c R.R + b R + a I
+    Z = free_buf(R, Q, -1);
+    if ((rc = launch(sym(p.S[R], p.S[R], p.S[Z], p.s, p.S[R], hp.c, hp.b, hp.a, nullptr))) != DION3_OK) return rc;
+    if (Q < 0) {
+      Q = Z;  // Q <- Z
+    } else {
+      const int nq = free_buf(R, Q, Z);
+      if ((rc = launch(sym(p.S[Z], p.S[Q], p.S[nq], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
+      Q = nq;
+    }
+    if (t < T && t + 1 != rs) {
+      // R <- Z (R Z); Z may be the buffer Q now points at, which is only read.
+      const int tm = free_buf(R, Q, Z);
+      if ((rc = launch(sym(p.S[R], p.S[Z], p.S[tm], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
+      if ((rc = launch(sym(p.S[Z], p.S[tm], p.S[R], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
+    }
+  }
+  // O = Q Y, written as X's k x m orientation.
+  GemmDesc g{};
+  g.A = p.Yt[ycur]; g.a_bstride = p.yt_bs; g.lda = p.sp;
+  g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
+  g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
+  g.mode = kRect; g.alpha = 1.f;
+  if (p.wide) {
+    g.outT = out.O; g.outT_bstride = out.o_bs; g.ld_outT = out.ld_o;
+  } else {
+    g.out = out.O; g.out_bstride = out.o_bs; g.ld_out = out.ld_o;
+  }
+  return launch(g);
+}
+
+// Step workspace layout for one group.
+struct GroupPlan {
+  int n, m, batch, k;
+  float* l1;
+  float* sq;
+  int32_t* idx;
+  float* fro2;
+  __half* O;
+  long long o_bs;
+  int ld_o;
+  NsPlan ns;
+};
+
+void plan_group(Carver& c, const dion3_group& g, float f, GroupPlan& gp) {
+  gp.n = g.rows;
+  gp.m = g.cols;
+  gp.batch = g.batch;
+  gp.k = num_selected(f, g.rows);
+  gp.l1 = c.take<float>(static_cast<long long>(g.batch) * g.rows);
+  gp.sq = c.take<float>(static_cast<long long>(g.batch) * g.rows);
+  gp.idx = c.take<int32_t>(static_cast<long long>(g.batch) * gp.k);
+  gp.fro2 = c.take<float>(g.batch);
+  gp.ld_o = static_cast<int>(round_up(g.cols, 8));
+  gp.o_bs = static_cast<long long>(gp.k) * gp.ld_o;
+  gp.O = c.take<__half>(gp.o_bs * g.batch);
+  plan_ns(c, gp.k, gp.m, gp.batch, gp.ns);
+}
+
+dion3_status check_group(const dion3_group& g, int gi) {
+  if (g.rows < 1 || g.cols < 1 || g.batch < 1)
+    return fail(DION3_ERR_INVALID_ARG, "group %d: rows, cols and batch must be >= 1", gi);
+  if (g.batch > 65535) return fail(DION3_ERR_INVALID_ARG, "group %d: batch > 65535", gi);
+  if (static_cast<long long>(g.rows) * g.cols > (1LL << 40))
+    return fail(DION3_ERR_INVALID_ARG, "group %d: matrix too large", gi);
+  if (g.param_dtype != DION3_F32 && g.param_dtype != DION3_BF16)
+    return fail(DION3_ERR_INVALID_ARG, "group %d: param_dtype must be DION3_F32 or DION3_BF16", gi);
+  if (g.grad_dtype != DION3_F32 && g.grad_dtype != DION3_BF16)
+    return fail(DION3_ERR_INVALID_ARG, "group %d: grad_dtype must be DION3_F32 or DION3_BF16", gi);
+  if (g.params == nullptr || g.grads == nullptr || g.momentum == nullptr)
+    return fail(DION3_ERR_INVALID_ARG, "group %d: pointer arrays must not be NULL", gi);
+  for (int b = 0; b < g.batch; ++b) {
+    if (g.params[b] == nullptr || g.grads[b] == nullptr || g.momentum[b] == nullptr)
+      return fail(DION3_ERR_INVALID_ARG, "group %d matrix %d: NULL tensor pointer", gi, b);
+    if (!aligned16(g.params[b]) || !aligned16(g.grads[b]) || !aligned16(g.momentum[b]))
+      return fail(DION3_ERR_INVALID_ARG, "group %d matrix %d: tensor pointers must be 16-byte aligned", gi, b);
+  }
+  return DION3_OK;
+}
+
+dion3_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need > 0 && ws == nullptr) return fail(DION3_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(DION3_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < need) return fail(DION3_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return DION3_OK;
+}
+
+}  // namespace
+}  // namespace dion3
+
+using namespace dion3;
+
+extern "C" {
+
+size_t dion3_abi_version(void) { return DION3_ABI_VERSION; }
+
+const char* dion3_status_string(int status) {
+  switch (status) {
+    case DION3_OK: return "DION3_OK";
+    case DION3_ERR_INVALID_ARG: return "DION3_ERR_INVALID_ARG";
+    case DION3_ERR_UNSUPPORTED: return "DION3_ERR_UNSUPPORTED";
+    case DION3_ERR_WORKSPACE: return "DION3_ERR_WORKSPACE";
+    case DION3_ERR_CUDA: return "DION3_ERR_CUDA";
+    case DION3_ERR_TIMEOUT: return "DION3_ERR_TIMEOUT";
+    case DION3_ERR_DEVICE_CHECK: return "DION3_ERR_DEVICE_CHECK";
+    default: return "unknown dion3 status";
+  }
+}
+
+const char* dion3_last_error(void) { return t_last_error.c_str(); }
+
+int32_t dion3_num_selected(float f, int32_t rows) { return dion3::num_selected(f, rows); }
+
+double dion3_useful_flops(int32_t k, int32_t m, const dion3_hparams* hp) {
+  if (k < 1 || m < 1 || check_hparams(hp, false) != DION3_OK) return -1.0;
+  return schedule_flops(k, m, *hp);
+}
+
+dion3_status dion3_select_workspace_size(int32_t rows, int32_t cols, int32_t batch, int32_t k, size_t* bytes) {
+  if (bytes == nullptr) return fail(DION3_ERR_INVALID_ARG, "bytes is NULL");
+  if (rows < 1 || cols < 1 || batch < 1 || k < 1 || k > rows)
+    return fail(DION3_ERR_INVALID_ARG, "need rows, cols, batch >= 1 and 1 <= k <= rows");
+  Carver c{nullptr};
+  c.take<float>(static_cast<long long>(batch) * rows);
+  c.take<float>(static_cast<long long>(batch) * rows);
+  *bytes = round_up(static_cast<long long>(c.off), 256);
+  return ok();
+}
+
+dion3_status dion3_select_rows(int32_t rows, int32_t cols, int32_t batch, float* const* momentum,
+                               const void* const* grads, int32_t grad_dtype, int32_t k, int32_t* idx_out,
+                               float* fro2_out, void* ws, size_t ws_bytes, dion3_stream_t stream) {
+  size_t need = 0;
+  dion3_status rc = dion3_select_workspace_size(rows, cols, batch, k, &need);
+  if (rc != DION3_OK) return rc;
+  if (batch > 65535) return fail(DION3_ERR_INVALID_ARG, "batch > 65535");
+  if (momentum == nullptr || idx_out == nullptr) return fail(DION3_ERR_INVALID_ARG, "momentum and idx_out must not be NULL");
+  if (grads != nullptr && grad_dtype != DION3_F32 && grad_dtype != DION3_BF16)
+    return fail(DION3_ERR_INVALID_ARG, "grad_dtype must be DION3_F32 or DION3_BF16");
+  for (int b = 0; b < batch; ++b) {
+    if (momentum[b] == nullptr || !aligned16(momentum[b]))
+      return fail(DION3_ERR_INVALID_ARG, "momentum[%d] NULL or not 16-byte aligned", b);
+    if (grads != nullptr && (grads[b] == nullptr || !aligned16(grads[b])))
+      return fail(DION3_ERR_INVALID_ARG, "grads[%d] NULL or not 16-byte aligned", b);
+  }
+  if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carver c{static_cast<char*>(ws)};
+  float* l1 = c.take<float>(static_cast<long long>(batch) * rows);
+  float* sq = c.take<float>(static_cast<long long>(batch) * rows);
+  const bool vec = cols % 8 == 0;
+  for (int b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+    const int nb = std::min(kMaxBatchPerLaunch, batch - b0);
+    AccumArgs a{};
+    a.rows = rows; a.cols = cols; a.batch = nb; a.grad_dtype = grad_dtype;
+    for (int i = 0; i < nb; ++i) {
+      a.M[i] = momentum[b0 + i];
+      a.G[i] = grads ? grads[b0 + i] : nullptr;
+    }
+    a.l1 = l1 + static_cast<size_t>(b0) * rows;
+    a.sq = sq + static_cast<size_t>(b0) * rows;
+    const cudaError_t e = launch_accum_rownorm(a, vec, s);
+    if (e != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
+  }
+  TopkArgs t{};
+  t.rows = rows; t.k = k; t.batch = batch; t.l1 = l1; t.sq = sq; t.idx = idx_out; t.fro2 = fro2_out;
+  const cudaError_t e = launch_topk(t, s);
+  if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+  return ok();
+}
+
+dion3_status dion3_gram_ns_workspace_size(int32_t k, int32_t m, int32_t batch, const dion3_hparams* hp,
+                                          size_t* bytes) {
+  if (bytes == nullptr) return fail(DION3_ERR_INVALID_ARG, "bytes is NULL");
+  if (k < 1 || m < 1 || batch < 1 || batch > 65535)
+    return fail(DION3_ERR_INVALID_ARG, "need k, m >= 1 and 1 <= batch <= 65535");
+  dion3_status rc = check_hparams(hp, false);
+  if (rc != DION3_OK) return rc;
+  Carver c{nullptr};
+  NsPlan p;
+  plan_ns(c, k, m, batch, p);
+  c.take<float>(static_cast<long long>(batch) * 64);
+  *bytes = round_up(static_cast<long long>(c.off), 256);
+  return ok();
+}
+
+dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const void* X, void* O,
+                                   const dion3_hparams* hp, void* ws, size_t ws_bytes, dion3_stream_t stream) {
+  size_t need = 0;
+  dion3_status rc = dion3_gram_ns_workspace_size(k, m, batch, hp, &need);
+  if (rc != DION3_OK) return rc;
+  if (X == nullptr || O == nullptr) return fail(DION3_ERR_INVALID_ARG, "X and O must not be NULL");
+  if (!aligned16(X) || !aligned16(O)) return fail(DION3_ERR_INVALID_ARG, "X and O must be 16-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carver c{static_cast<char*>(ws)};
+  NsPlan p;
+  plan_ns(c, k, m, batch, p);
+  constexpr int kParts = 64;
+  float* parts = c.take<float>(static_cast<long long>(batch) * kParts);
+  const long long n = static_cast<long long>(k) * m;
+  cudaError_t e = launch_sumsq_f16(static_cast<const __half*>(X), n, batch, parts, kParts, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sumsq launch");
+  GatherArgs g{};
+  g.k = k; g.m = m; g.batch = batch; g.src_f32 = false;
+  g.X = static_cast<const __half*>(X);
+  g.fro2 = parts; g.fro2_parts = kParts; g.eps = hp->eps; g.decay = false;
+  g.n = k; g.status = st;
+  gather_targets(p, g);
+  e = launch_gather(g, m % 4 == 0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  NsOut out{static_cast<__half*>(O), static_cast<long long>(k) * m, m};
+  if ((rc = run_gram_ns(p, *hp, out, st, s)) != DION3_OK) return rc;
+  return ok();
+}
+
+dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp,
+                                  size_t* bytes) {
+  if (bytes == nullptr) return fail(DION3_ERR_INVALID_ARG, "bytes is NULL");
+  if (groups == nullptr || ngroups < 1) return fail(DION3_ERR_INVALID_ARG, "need ngroups >= 1 groups");
+  dion3_status rc = check_hparams(hp, true);
+  if (rc != DION3_OK) return rc;
+  Carver c{nullptr};
+  for (int i = 0; i < ngroups; ++i) {
+    if (groups[i].rows < 1 || groups[i].cols < 1 || groups[i].batch < 1 || groups[i].batch > 65535)
+      return fail(DION3_ERR_INVALID_ARG, "group %d: rows, cols >= 1 and 1 <= batch <= 65535 required", i);
+    GroupPlan gp;
+    plan_group(c, groups[i], hp->f, gp);
+  }
+  *bytes = round_up(static_cast<long long>(c.off), 256);
+  return ok();
+}
+
+dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp, void* ws,
+                        size_t ws_bytes, int32_t* const* sel_idx_out, dion3_stream_t stream) {
+  size_t need = 0;
+  dion3_status rc = dion3_workspace_size(groups, ngroups, hp, &need);
+  if (rc != DION3_OK) return rc;
+  for (int i = 0; i < ngroups; ++i)
+    if ((rc = check_group(groups[i], i)) != DION3_OK) return rc;
+  if (sel_idx_out != nullptr)
+    for (int i = 0; i < ngroups; ++i)
+      if (sel_idx_out[i] != nullptr && (reinterpret_cast<uintptr_t>(sel_idx_out[i]) & 3u))
+        return fail(DION3_ERR_INVALID_ARG, "sel_idx_out[%d] must be 4-byte aligned", i);
+  if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float lr_eff = static_cast<float>(static_cast<double>(hp->lr) / std::sqrt(static_cast<double>(hp->f)));
+  Carver c{static_cast<char*>(ws)};
+  for (int gi = 0; gi < ngroups; ++gi) {
+    const dion3_group& g = groups[gi];
+    GroupPlan gp;
+    plan_group(c, g, hp->f, gp);
+    int32_t* idx = (sel_idx_out != nullptr && sel_idx_out[gi] != nullptr) ? sel_idx_out[gi] : gp.idx;
+    const bool vec = g.cols % 8 == 0;
+    cudaError_t e;
+    // (a) accumulate + norms, then top-k.
+    for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
+      const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
+      AccumArgs a{};
+      a.rows = g.rows; a.cols = g.cols; a.batch = nb; a.grad_dtype = g.grad_dtype;
+      for (int i = 0; i < nb; ++i) {
+        a.M[i] = g.momentum[b0 + i];
+        a.G[i] = g.grads[b0 + i];
+      }
+      a.l1 = gp.l1 + static_cast<size_t>(b0) * g.rows;
+      a.sq = gp.sq + static_cast<size_t>(b0) * g.rows;
+      if ((e = launch_accum_rownorm(a, vec, s)) != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
+    }
+    TopkArgs t{};
+    t.rows = g.rows; t.k = gp.k; t.batch = g.batch; t.l1 = gp.l1; t.sq = gp.sq; t.idx = idx; t.fro2 = gp.fro2;
+    if ((e = launch_topk(t, s)) != cudaSuccess) return cuda_fail(e, "topk launch");
+    // (b) gather/normalise (+ decay of the selected momentum rows), Gram-NS.
+    for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
+      const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
+      GatherArgs ga{};
+      ga.k = gp.k; ga.m = g.cols; ga.batch = nb; ga.src_f32 = true;
+      for (int i = 0; i < nb; ++i) ga.M[i] = g.momentum[b0 + i];
+      ga.idx = idx + static_cast<size_t>(b0) * gp.k;
+      ga.fro2 = gp.fro2 + b0; ga.fro2_parts = 1; ga.eps = hp->eps; ga.mu = hp->mu; ga.decay = true;
+      ga.n = g.rows; ga.status = st;
+      gather_targets(gp.ns, ga);
+      ga.out_rows += ga.rows_bstride * b0;
+      ga.out_cols += ga.cols_bstride * b0;
+      if ((e = launch_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
+    }
+    NsOut out{gp.O, gp.o_bs, gp.ld_o};
+    if ((rc = run_gram_ns(gp.ns, *hp, out, st, s)) != DION3_OK) return rc;
+    // (c) scatter update of the selected parameter rows.
+    for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
+      const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
+      ScatterArgs sa{};
+      sa.rows = g.rows; sa.cols = g.cols; sa.k = gp.k; sa.batch = nb; sa.param_dtype = g.param_dtype;
+      for (int i = 0; i < nb; ++i) sa.W[i] = g.params[b0 + i];
+      sa.idx = idx + static_cast<size_t>(b0) * gp.k;
+      sa.O = gp.O + gp.o_bs * b0; sa.o_bstride = gp.o_bs; sa.ld_o = gp.ld_o;
+      sa.lr = lr_eff;
+      sa.status = st;
+      if ((e = launch_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
+    }
+  }
+  return ok();
+}
+
+dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t batch, const void* A,
+                            int32_t lda, int64_t a_bstride, const void* B, int32_t ldb, int64_t b_bstride,
+                            const void* C, int32_t ldc, int64_t c_bstride, void* D, int32_t ldd,
+                            int64_t d_bstride, void* DT, int32_t lddt, int64_t dt_bstride, float alpha,
+                            float beta, float gamma, dion3_stream_t stream) {
+  if (mode != DION3_GEMM_RECT && mode != DION3_GEMM_SYM_LOWER) return fail(DION3_ERR_INVALID_ARG, "bad GEMM mode");
+  if (M < 1 || N < 1 || K < 1 || batch < 1 || batch > 65535)
+    return fail(DION3_ERR_INVALID_ARG, "need M, N, K >= 1 and 1 <= batch <= 65535");
+  if (mode == DION3_GEMM_SYM_LOWER && (M != N || D == nullptr || DT != nullptr))
+    return fail(DION3_ERR_INVALID_ARG, "symmetric mode needs M == N, D set and DT NULL");
+  if (D == nullptr && DT == nullptr) return fail(DION3_ERR_INVALID_ARG, "no output given");
+  if (D != nullptr && ldd < N) return fail(DION3_ERR_INVALID_ARG, "ldd < N");
+  if (DT != nullptr && lddt < M) return fail(DION3_ERR_INVALID_ARG, "lddt < M");
+  if (C != nullptr && ldc < N) return fail(DION3_ERR_INVALID_ARG, "ldc < N");
+  if (((reinterpret_cast<uintptr_t>(D) | reinterpret_cast<uintptr_t>(DT) | reinterpret_cast<uintptr_t>(C)) & 1u) != 0)
+    return fail(DION3_ERR_INVALID_ARG, "C, D and DT must be 2-byte aligned");
+  if (batch > 1 && (a_bstride < static_cast<int64_t>(lda) * M || b_bstride < static_cast<int64_t>(ldb) * N))
+    return fail(DION3_ERR_INVALID_ARG, "operand batch stride smaller than one matrix");
+  GemmDesc g{};
+  g.A = static_cast<const __half*>(A); g.a_bstride = a_bstride; g.lda = lda;
+  g.B = static_cast<const __half*>(B); g.b_bstride = b_bstride; g.ldb = ldb;
+  g.M = M; g.N = N; g.K = K; g.batch = batch;
+  g.mode = mode == DION3_GEMM_SYM_LOWER ? kSymLower : kRect;
+  g.alpha = alpha; g.beta = beta; g.gamma = gamma;
+  g.C = static_cast<const __half*>(C); g.c_bstride = c_bstride; g.ldc = ldc;
+  g.out = static_cast<__half*>(D); g.out_bstride = d_bstride; g.ld_out = ldd;
+  g.outT = static_cast<__half*>(DT); g.outT_bstride = dt_bstride; g.ld_outT = lddt;
+  const char* why = nullptr;
+  if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "%s", why);
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+  const cudaError_t e = launch_gemm(g, st, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+  return ok();
+}
+
+dion3_status dion3_device_status(dion3_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+  unsigned v = 0;
+  if ((e = cudaMemcpy(&v, st, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "status read");
+  const unsigned zero = 0;
+  if ((e = cudaMemcpy(st, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "status clear");
+  if (v & kDevTimeout) return fail(DION3_ERR_TIMEOUT, "a bounded device-side wait ran out");
+  if (v & kDevCheck) return fail(DION3_ERR_DEVICE_CHECK, "a device-side check failed");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,473 @@
+// Tensor-core GEMM for the Gram Newton-Schulz path on sm_103a.
+//
+// D = A B^T with A [batch][M][K] and B [batch][N][K] in fp16, both K-major,
+// fp32 accumulation in tensor memory, and the epilogue
+//     v = alpha D + beta C + gamma I
+// rounded to fp16.  In kSymLower mode only the lower-triangle tiles of the
+// (symmetric) M x M result are computed; each tile is written in place and
+// mirrored into the upper triangle, so the stored matrix is exactly
+// symmetric.  In kRect mode every tile is computed and written in the normal
+// and/or the transposed orientation.
+//
+// Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of the
+// paper).  First-level paragraph: Newton-Schulz iterates on the small
+// symmetric Gram matrix X X^T and multiplies back by X at the end.  Second-level
+// paragraph: the symmetric products A^T A and A^2 + B only need the lower
+// triangle, copied to the upper one.  The products used here:
+//   R = Y Y^T          (A = B = Y, kSymLower)
+//   Z = cR.R + bR + aI (A = B = R, C = R, kSymLower)
+//   Q <- Z Q, T = R Z, R <- Z T  (B symmetric, so B^T = B; kSymLower)
+//   Y_new^T = Y^T Q, O = (Y^T Q)^T  (A = Y^T, B = Q, kRect)
+//
+// Data path per CTA (one 128 x BN output tile, 4 warps):
+//   warp 0 lane 0: TMA producer, 128-byte-swizzled 64-wide K slabs of A and B
+//                  into a STAGES-deep shared-memory ring (mbarrier expect_tx);
+//   warp 1 lane 0: issues tcgen05.mma (cta_group::1, kind::f16, M=128, N=BN,
+//                  K=16) into a BN-column TMEM accumulator; tcgen05.commit
+//                  frees each ring slot and finally signals the epilogue;
+//   all 4 warps:   tcgen05.ld 32 lanes x 32 columns per warp, epilogue, stores.
+// Every mbarrier wait is bounded (about one second, %globaltimer); a wait that
+// runs out sets a bit in the device status word and the CTA winds down (the
+// TMEM it holds is freed on every path).
+#include "internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace dion3 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // fp16 elements per 128-byte swizzle row
+constexpr int kThreads = 128;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+struct GemmParams {
+  int M, N, K, mode, tiles_n;
+  float alpha, beta, gamma;
+  const __half* C; long long c_bs; int ldc;
+  __half* out; long long out_bs; int ld_out;
+  __half* outT; long long outT_bs; int ld_outT;
+  unsigned* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Bounded wait for the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kDevTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) core groups
+// stacked along M/N (stride-dimension byte offset 1024), descriptor version 1
+// (bits 46-47), swizzle mode 2 = 128B (bits 61-63).  The leading-dimension
+// offset is not used for swizzled K-major layouts whose MMA K extent (32 bytes)
+// lies inside one swizzle row; it is set to 1 (16 bytes).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+template <int N>
+__device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+// Lower-triangle tile t -> (i, j), i >= j, t = i (i + 1) / 2 + j.
+__device__ __forceinline__ void tri_tile(int t, int& i, int& j) {
+  int r = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
+  while ((r + 1) * (r + 2) / 2 <= t) ++r;
+  while (r * (r + 1) / 2 > t) --r;
+  i = r;
+  j = t - r * (r + 1) / 2;
+}
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kBarBytes = (2 * STAGES + 1) * 8;
+  static constexpr int kDynSmem = 1024 /*alignment slack*/ + kRingBytes + kBarBytes + 16;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ GemmParams p) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + STAGES * L::kABytes;
+  const uint32_t bar_full = base + L::kRingBytes;
+  const uint32_t bar_empty = bar_full + STAGES * 8;
+  const uint32_t bar_acc = bar_empty + STAGES * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kRingBytes + L::kBarBytes);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bidx = blockIdx.y;
+  int tm, tn;
+  if (p.mode == kSymLower) {
+    tri_tile(blockIdx.x, tm, tn);
+  } else {
+    tm = blockIdx.x / p.tiles_n;
+    tn = blockIdx.x % p.tiles_n;
+  }
+  const int m0 = tm * BM, n0 = tn * BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), BN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nkb = (p.K + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer.
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
+      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, p.status)) break;
+      mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
+      tma_load_3d(sA + s * L::kABytes, &tmA, bar_full + 8 * s, kb * BK, m0, bidx);
+      tma_load_3d(sB + s * L::kBBytes, &tmB, bar_full + 8 * s, kb * BK, n0, bidx);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer.
+    constexpr uint32_t idesc = idesc_f16_f32<BN>();
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
+      if (!mbar_wait(bar_full + 8 * s, ph, p.status)) break;
+      tc_fence_after();
+      const uint64_t da = sdesc_kmajor_sw128(sA + s * L::kABytes);
+      const uint64_t db = sdesc_kmajor_sw128(sB + s * L::kBBytes);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        // +32 bytes along K inside the swizzle row = +2 in the address field.
+        mma_f16_ss(tmem, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_empty + 8 * s);
+    }
+    mma_commit(bar_acc);
+  }
+  __syncwarp();
+
+  // Epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w + 31.
+  // Warp-uniform outcome, so the .sync.aligned TMEM loads below never run in a
+  // partially active warp.
+  const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0u, p.status));
+  tc_fence_after();
+  if (acc_ok) {
+    const int r = m0 + warp * 32 + lane;
+    const bool sym = p.mode == kSymLower;
+    const bool diag = sym && (tm == tn);
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    __half* outb = p.out ? p.out + static_cast<long long>(bidx) * p.out_bs : nullptr;
+    __half* tb = sym ? outb : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
+    const int ldt = sym ? p.ld_out : p.ld_outT;
+    const __half* cb = p.C ? p.C + static_cast<long long>(bidx) * p.c_bs : nullptr;
+    for (int cc = 0; cc < BN; cc += 32) {
+      if (n0 + cc >= p.N) break;  // uniform across the CTA
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(trow + static_cast<uint32_t>(cc), v);
+      tmem_ld_wait();
+      if (r >= p.M) continue;
+      const int c0 = n0 + cc;
+      const bool full = (c0 + 32 <= p.N);
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
+      if (cb != nullptr) {
+        const __half* crow = cb + static_cast<size_t>(r) * p.ldc + c0;
+        if (full && (p.ldc % 8 == 0)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = *reinterpret_cast<const uint4*>(crow + 8 * q);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 x = __half22float2(h2[e]);
+              f[8 * q + 2 * e] = fmaf(p.beta, x.x, f[8 * q + 2 * e]);
+              f[8 * q + 2 * e + 1] = fmaf(p.beta, x.y, f[8 * q + 2 * e + 1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < p.N) f[j] = fmaf(p.beta, __half2float(crow[j]), f[j]);
+        }
+      }
+      if (p.gamma != 0.0f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (r == c0 + j) f[j] += p.gamma;
+      }
+      uint32_t hp[16];  // 32 fp16 values, two per word
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const __half2 t = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+        hp[j] = *reinterpret_cast<const uint32_t*>(&t);
+      }
+
+      if (outb != nullptr) {
+        __half* dst = outb + static_cast<size_t>(r) * p.ld_out + c0;
+        if (!diag && full && (p.ld_out % 8 == 0)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < p.N && (!diag || r >= c0 + j))
+              dst[j] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+        }
+      }
+      if (tb != nullptr) {
+        // Mirror (symmetric) or transposed write: for a fixed column the warp's
+        // 32 lanes write 32 consecutive elements of one output row.
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int c = c0 + j;
+          if (c < p.N && (!diag || r > c))
+            tb[static_cast<size_t>(c) * ldt + r] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+constexpr int kBN = 128;
+constexpr int kStages = 4;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D tensor map over [batch][rows][cols] fp16 with row pitch `ld` elements,
+// box = 64 columns x box_rows rows x 1 matrix, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, int rows, int cols, int batch,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, static_cast<cuuint64_t>(bstride) * 2u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_check(const GemmDesc& g, const char** why) {
+  auto fail = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batch <= 0) return fail("gemm: empty dimension");
+  if (g.A == nullptr || g.B == nullptr) return fail("gemm: null operand");
+  if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B)) & 15u)
+    return fail("gemm: operands must be 16-byte aligned");
+  if (g.lda % 8 || g.ldb % 8 || g.a_bstride % 8 || g.b_bstride % 8)
+    return fail("gemm: operand pitches must be multiples of 8 elements");
+  if (g.lda < g.K || g.ldb < g.K) return fail("gemm: pitch smaller than K");
+  if (g.mode == kSymLower && (g.M != g.N || g.out == nullptr)) return fail("gemm: symmetric mode needs M == N and out");
+  if (g.mode == kRect && g.out == nullptr && g.outT == nullptr) return fail("gemm: no output");
+  if (g.M > (1 << 24) || g.N > (1 << 24)) return fail("gemm: dimension too large");
+  return true;
+}
+
+cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
+  using L = Layout<kBN, kStages>;
+  auto kern = gemm_tcgen05_kernel<kBN, kStages>;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, kBN)) return cudaErrorInvalidValue;
+
+  GemmParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.mode = g.mode;
+  const int tiles_m = (g.M + BM - 1) / BM;
+  const int tiles_n = (g.N + kBN - 1) / kBN;
+  p.tiles_n = tiles_n;
+  p.alpha = g.alpha;
+  p.beta = g.beta;
+  p.gamma = g.gamma;
+  p.C = g.C;
+  p.c_bs = g.c_bstride;
+  p.ldc = g.ldc;
+  p.out = g.out;
+  p.out_bs = g.out_bstride;
+  p.ld_out = g.ld_out;
+  p.outT = g.outT;
+  p.outT_bs = g.outT_bstride;
+  p.ld_outT = g.ld_outT;
+  p.status = dev_status;
+
+  long long ntiles;
+  if (g.mode == kSymLower) {
+    // BM == kBN, so the tile grid is square.
+    ntiles = static_cast<long long>(tiles_m) * (tiles_m + 1) / 2;
+  } else {
+    ntiles = static_cast<long long>(tiles_m) * tiles_n;
+  }
+  if (ntiles > 0x7fffffffLL || g.batch > 65535) return cudaErrorInvalidConfiguration;
+  kern<<<dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(g.batch)), kThreads, L::kDynSmem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dion3

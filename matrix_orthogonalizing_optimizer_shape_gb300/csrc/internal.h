@@ -1,0 +1,110 @@
+// Internal launcher interface shared by the library's translation units.
+// Nothing here crosses the C ABI (include/dion3.h is the public surface).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace dion3 {
+
+// Device status word bits (written by bounded device-side waits and checks).
+enum : unsigned { kDevTimeout = 1u, kDevCheck = 2u };
+
+// Matrices per launch of the pointer-table kernels (keeps parameters < 4 KB).
+constexpr int kMaxBatchPerLaunch = 96;
+
+enum DType : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+// ---------------------------------------------------------------------------
+// Memory-bound kernels (mem_kernels.cu)
+// ---------------------------------------------------------------------------
+
+// a0: M <- M + G (if G given) and per-row l1 / sum of squares of the new M.
+struct AccumArgs {
+  int rows, cols, batch;             // batch <= kMaxBatchPerLaunch
+  int grad_dtype;                    // kF32 or kBF16
+  float* M[kMaxBatchPerLaunch];
+  const void* G[kMaxBatchPerLaunch]; // all null: norms only
+  float* l1;                         // [batch][rows]
+  float* sq;                         // [batch][rows]
+};
+cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s);
+
+// a1: top-k rows by l1 (ties to the lower index), indices ascending, and
+// fro2 = sum of sq over the selected rows.
+struct TopkArgs {
+  int rows, k, batch;
+  const float* l1;   // [batch][rows]
+  const float* sq;   // [batch][rows]
+  int32_t* idx;      // [batch][k]
+  float* fro2;       // [batch] (may be null)
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+
+// a2: gather + normalise (+ optional decay of the source rows) into fp16, in
+// both orientations: rows-major [k][ld_rows] and columns-major [m][ld_cols].
+struct GatherArgs {
+  int n;                           // rows of each source matrix (bounds check of idx)
+  int k, m, batch;                 // batch <= kMaxBatchPerLaunch when src_f32
+  bool src_f32;                    // true: rows of fp32 M picked by idx; false: fp16 X
+  float* M[kMaxBatchPerLaunch];    // src_f32: momentum pointers
+  const int32_t* idx;              // src_f32: [batch][k]
+  const __half* X;                 // !src_f32: [batch][k][m] contiguous
+  const float* fro2;               // [batch][fro2_parts]
+  int fro2_parts;
+  float eps;
+  float mu;                        // decay applied to the source rows (src_f32)
+  bool decay;
+  unsigned* status;                // device status word (kDevCheck on a bad index)
+  __half* out_rows; long long rows_bstride; int ld_rows;   // [k][ld_rows]
+  __half* out_cols; long long cols_bstride; int ld_cols;   // [m][ld_cols]
+};
+cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s);
+
+// Sum of squares of fp16 X [batch][n] into parts [batch][parts].
+cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts,
+                             int nparts, cudaStream_t s);
+
+// a7: W[S_i] <- round(W[S_i] - lr O[i]) for the selected rows.
+struct ScatterArgs {
+  int rows, cols, k, batch;        // batch <= kMaxBatchPerLaunch
+  int param_dtype;                 // kF32 or kBF16
+  void* W[kMaxBatchPerLaunch];
+  const int32_t* idx;              // [batch][k]
+  const __half* O; long long o_bstride; int ld_o;   // [k][ld_o]
+  float lr;
+  unsigned* status;                // device status word (kDevCheck on a bad index)
+};
+cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Tensor-core GEMM (gemm_tcgen05.cu): D = A B^T with A [batch][M][K] and
+// B [batch][N][K] fp16 (K contiguous), fp32 accumulation in TMEM, and the
+// epilogue  v = alpha D + beta C + gamma I  written as fp16.
+// ---------------------------------------------------------------------------
+enum GemmMode : int {
+  kRect = 0,      // every tile; write `out` (normal) and/or `outT` (transposed)
+  kSymLower = 1,  // M == N, lower-triangle tiles only; `out` gets the tile and its mirror
+};
+
+struct GemmDesc {
+  const __half* A; long long a_bstride; int lda;
+  const __half* B; long long b_bstride; int ldb;
+  int M, N, K, batch;
+  int mode;
+  float alpha, beta, gamma;
+  const __half* C; long long c_bstride; int ldc;     // may be null (beta ignored)
+  __half* out; long long out_bstride; int ld_out;    // may be null in kRect
+  __half* outT; long long outT_bstride; int ld_outT; // may be null
+};
+
+// Host-side checks of a descriptor (alignment and pitch rules of the TMA
+// tensor maps); returns false with a message if the GEMM cannot be launched.
+bool gemm_check(const GemmDesc& g, const char** why);
+cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s);
+
+// Status word address on the current device (set up by the API unit).
+unsigned* device_status_ptr();
+
+}  // namespace dion3

@@ -1,0 +1,492 @@
+// Memory-bound kernels of the Dion3 step: momentum accumulation with row
+// norms, l1 top-k selection, gather/normalise/transpose into fp16, the sum of
+// squares used for normalisation, and the row-scatter parameter update.
+//
+// Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of
+// the paper), third-level paragraph: rows are chosen by l1 norm, k = ceil(f n),
+// only the chosen sub-matrix is orthogonalised and only the matching weight
+// rows are updated; error feedback decays only the chosen momentum rows by mu.
+#include "internal.h"
+
+#include <cuda_bf16.h>
+
+namespace dion3 {
+namespace {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ float load_grad(const void* g, size_t i, int gd) {
+  if (gd == kBF16) {
+    const uint16_t h = reinterpret_cast<const uint16_t*>(g)[i];
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  return reinterpret_cast<const float*>(g)[i];
+}
+
+// ---------------------------------------------------------------------------
+// a0: M <- M + G and per-row l1 / sum of squares.  One warp per row; the
+// vector path moves 8 elements per lane per iteration (two float4 of M, one
+// 16-byte bf16 or two float4 fp32 gradient loads) and keeps UNROLL iterations
+// of loads in flight before the first dependent store.
+// ---------------------------------------------------------------------------
+template <bool VEC, int GD>  // GD: kF32, kBF16, or -1 (no gradient: norms only)
+__global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constant__ AccumArgs a) {
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const long long total = static_cast<long long>(a.batch) * a.rows;
+  if (gw >= total) return;
+  const int b = static_cast<int>(gw / a.rows);
+  const int r = static_cast<int>(gw % a.rows);
+  const int cols = a.cols;
+  float* __restrict__ Mrow = a.M[b] + static_cast<size_t>(r) * cols;
+  float l1 = 0.f, sq = 0.f;
+
+  if constexpr (VEC) {
+    constexpr int U = 4;  // iterations of loads kept in flight
+    const int step = kWarp * 8;
+    for (int c0 = lane * 8; c0 < cols; c0 += step * U) {
+      float m[U][8];
+      float g[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * step;
+        if (c < cols) {
+          const float4 x0 = *reinterpret_cast<const float4*>(Mrow + c);
+          const float4 x1 = *reinterpret_cast<const float4*>(Mrow + c + 4);
+          m[u][0] = x0.x; m[u][1] = x0.y; m[u][2] = x0.z; m[u][3] = x0.w;
+          m[u][4] = x1.x; m[u][5] = x1.y; m[u][6] = x1.z; m[u][7] = x1.w;
+          if constexpr (GD == kBF16) {
+            const uint16_t* G = reinterpret_cast<const uint16_t*>(a.G[b]) + static_cast<size_t>(r) * cols;
+            bf16x8_to_f32(__ldcs(reinterpret_cast<const uint4*>(G + c)), g[u]);
+          } else if constexpr (GD == kF32) {
+            const float* G = reinterpret_cast<const float*>(a.G[b]) + static_cast<size_t>(r) * cols;
+            const float4 y0 = __ldcs(reinterpret_cast<const float4*>(G + c));
+            const float4 y1 = __ldcs(reinterpret_cast<const float4*>(G + c + 4));
+            g[u][0] = y0.x; g[u][1] = y0.y; g[u][2] = y0.z; g[u][3] = y0.w;
+            g[u][4] = y1.x; g[u][5] = y1.y; g[u][6] = y1.z; g[u][7] = y1.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * step;
+        if (c < cols) {
+          if constexpr (GD >= 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m[u][j] = __fadd_rn(m[u][j], g[u][j]);
+            *reinterpret_cast<float4*>(Mrow + c) = make_float4(m[u][0], m[u][1], m[u][2], m[u][3]);
+            *reinterpret_cast<float4*>(Mrow + c + 4) = make_float4(m[u][4], m[u][5], m[u][6], m[u][7]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            l1 += fabsf(m[u][j]);
+            sq = fmaf(m[u][j], m[u][j], sq);
+          }
+        }
+      }
+    }
+  } else {
+    for (int c = lane; c < cols; c += kWarp) {
+      float m = Mrow[c];
+      if constexpr (GD >= 0) {
+        m = __fadd_rn(m, load_grad(a.G[b], static_cast<size_t>(r) * cols + c, GD));
+        Mrow[c] = m;
+      }
+      l1 += fabsf(m);
+      sq = fmaf(m, m, sq);
+    }
+  }
+  l1 = warp_sum(l1);
+  sq = warp_sum(sq);
+  if (lane == 0) {
+    a.l1[gw] = l1;
+    a.sq[gw] = sq;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a1: top-k by l1.  One CTA per matrix.  l1 >= 0, so its fp32 bit pattern
+// orders like its value: a 4-pass 8-bit radix select finds the k-th largest
+// key t and how many of the keys equal to t are still needed; a single pass in
+// index order then keeps every key > t and the first `need` keys == t (ties go
+// to the lower index) and compacts the kept indices in ascending order.
+// ---------------------------------------------------------------------------
+constexpr int kTopkThreads = 1024;
+
+// Exclusive block-wide scan of one 0/1 flag per thread; returns the rank and
+// stores the block total in *total.
+__device__ __forceinline__ int block_excl_scan_flag(bool flag, int* warp_tot, int* total) {
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  const unsigned ball = __ballot_sync(0xffffffffu, flag);
+  const int in_warp = __popc(ball & ((1u << lane) - 1u));
+  if (lane == 0) warp_tot[warp] = __popc(ball);
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x / kWarp;
+    int v = lane < nw ? warp_tot[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane < nw) warp_tot[lane] = incl - v;  // exclusive
+    if (lane == nw - 1) *total = incl;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + in_warp;
+  __syncthreads();  // warp_tot is reused by the next call
+  return r;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_prefix;
+  __shared__ int s_need;
+  __shared__ int warp_tot[32];
+  __shared__ int tot_a, tot_b;
+  __shared__ float red[32];
+
+  const int b = blockIdx.x;
+  const int n = a.rows;
+  const unsigned* keys = reinterpret_cast<const unsigned*>(a.l1 + static_cast<size_t>(b) * n);
+  const float* sq = a.sq + static_cast<size_t>(b) * n;
+  const int tid = threadIdx.x;
+
+  unsigned prefix = 0u, mask = 0u;
+  int need = a.k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+      const unsigned u = keys[i];
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned above = 0u;
+      int d = 255;
+      for (; d > 0; --d) {
+        if (above + hist[d] >= static_cast<unsigned>(need)) break;
+        above += hist[d];
+      }
+      s_prefix = prefix | (static_cast<unsigned>(d) << shift);
+      s_need = need - static_cast<int>(above);
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+
+  // Compaction in index order.
+  int run_eq = 0, run_sel = 0;
+  float fsum = 0.f;
+  int32_t* out = a.idx + static_cast<size_t>(b) * a.k;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const bool valid = i < n;
+    const unsigned u = valid ? keys[i] : 0u;
+    const bool gt = valid && u > prefix;
+    const bool eq = valid && u == prefix;
+    const int eq_rank = run_eq + block_excl_scan_flag(eq, warp_tot, &tot_a);
+    const bool sel = gt || (eq && eq_rank < need);
+    const int pos = run_sel + block_excl_scan_flag(sel, warp_tot, &tot_b);
+    if (sel && pos < a.k) {
+      out[pos] = i;
+      fsum += sq[i];
+    }
+    run_eq += tot_a;
+    run_sel += tot_b;
+  }
+  if (a.fro2 != nullptr) {
+    fsum = warp_sum(fsum);
+    if (tid % kWarp == 0) red[tid / kWarp] = fsum;
+    __syncthreads();
+    if (tid < kWarp) {
+      float v = tid < static_cast<int>(blockDim.x / kWarp) ? red[tid] : 0.f;
+      v = warp_sum(v);
+      if (tid == 0) a.fro2[b] = v;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a2: gather + normalise into fp16, both orientations, with the error-feedback
+// decay of the source momentum rows fused in (the undecayed values are the
+// ones normalised).  Tile: 32 selected rows x 128 columns per CTA; each warp
+// reads one 512-byte row segment per pass; the column-major copy is staged
+// through shared memory so both outputs are written in contiguous runs.
+// ---------------------------------------------------------------------------
+constexpr int kGRows = 32, kGCols = 128;
+
+template <bool SRC_F32, bool VEC>
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherArgs a) {
+  __shared__ __align__(16) __half tile[kGCols][kGRows + 8];
+  const int b = blockIdx.z;
+  const int i0 = blockIdx.y * kGRows;
+  const int c0 = blockIdx.x * kGCols;
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+
+  float f2 = 0.f;
+  for (int p = 0; p < a.fro2_parts; ++p) f2 += a.fro2[static_cast<size_t>(b) * a.fro2_parts + p];
+  const float inv = 1.0f / (sqrtf(f2) + a.eps);
+
+  for (int rr = warp; rr < kGRows; rr += 256 / kWarp) {
+    const int i = i0 + rr;
+    const int c = c0 + lane * 4;
+    __half h[4] = {__float2half_rn(0.f), __float2half_rn(0.f), __float2half_rn(0.f), __float2half_rn(0.f)};
+    bool live = i < a.k && c < a.m;
+    int row = 0;
+    if constexpr (SRC_F32) {
+      if (i < a.k) {
+        row = a.idx[static_cast<size_t>(b) * a.k + i];
+        if (row < 0 || row >= a.n) {  // never expected: record it and skip the access
+          if (lane == 0) atomicOr(a.status, kDevCheck);
+          live = false;
+        }
+      }
+    }
+    if (live) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool full = VEC && (c + 4 <= a.m);
+      if constexpr (SRC_F32) {
+        float* src = a.M[b] + static_cast<size_t>(row) * a.m;
+        if (full) {
+          const float4 x = *reinterpret_cast<const float4*>(src + c);
+          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+          if (a.decay)
+            *reinterpret_cast<float4*>(src + c) =
+                make_float4(__fmul_rn(a.mu, x.x), __fmul_rn(a.mu, x.y), __fmul_rn(a.mu, x.z), __fmul_rn(a.mu, x.w));
+        } else {
+          for (int j = 0; j < 4; ++j)
+            if (c + j < a.m) {
+              v[j] = src[c + j];
+              if (a.decay) src[c + j] = __fmul_rn(a.mu, v[j]);
+            }
+        }
+      } else {
+        const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * a.m;
+        if (full) {
+          const uint2 x = *reinterpret_cast<const uint2*>(src + c);
+          const __half2 p0 = *reinterpret_cast<const __half2*>(&x.x);
+          const __half2 p1 = *reinterpret_cast<const __half2*>(&x.y);
+          v[0] = __low2float(p0); v[1] = __high2float(p0);
+          v[2] = __low2float(p1); v[3] = __high2float(p1);
+        } else {
+          for (int j = 0; j < 4; ++j)
+            if (c + j < a.m) v[j] = __half2float(src[c + j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = __float2half_rn(v[j] * inv);
+      __half* dst = a.out_rows + static_cast<long long>(b) * a.rows_bstride + static_cast<size_t>(i) * a.ld_rows + c;
+      if (full && (a.ld_rows % 4 == 0)) {
+        uint2 w;
+        __half2 q0 = __halves2half2(h[0], h[1]);
+        __half2 q1 = __halves2half2(h[2], h[3]);
+        w.x = *reinterpret_cast<uint32_t*>(&q0);
+        w.y = *reinterpret_cast<uint32_t*>(&q1);
+        *reinterpret_cast<uint2*>(dst) = w;
+      } else {
+        for (int j = 0; j < 4; ++j)
+          if (c + j < a.m) dst[j] = h[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tile[lane * 4 + j][rr] = h[j];
+  }
+  __syncthreads();
+
+  // Column-major copy: out_cols[c][i0 .. i0+32), 16 bytes per thread.  Rows
+  // in [k, ld_cols) are pitch padding and receive zeros.
+  for (int pass = 0; pass < 2; ++pass) {
+    const int cc = pass * 64 + threadIdx.x / 4;
+    const int seg = (threadIdx.x % 4) * 8;
+    const int c = c0 + cc;
+    const int i = i0 + seg;
+    if (c >= a.m || i >= a.ld_cols) continue;
+    __half* dst = a.out_cols + static_cast<long long>(b) * a.cols_bstride + static_cast<size_t>(c) * a.ld_cols + i;
+    if (i + 8 <= a.ld_cols && (a.ld_cols % 8 == 0)) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[cc][seg]);
+    } else {
+      for (int j = 0; j < 8 && i + j < a.ld_cols; ++j) dst[j] = tile[cc][seg + j];
+    }
+  }
+}
+
+// Sum of squares of fp16 X: grid (nparts, batch); part p covers a contiguous
+// chunk of matrix b.
+__global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long long n, float* parts, int nparts) {
+  __shared__ float red[8];
+  const int b = blockIdx.y, p = blockIdx.x;
+  const long long chunk = ((n + nparts - 1) / nparts + 7) / 8 * 8;
+  const long long lo = p * chunk;
+  const long long hi = lo + chunk < n ? lo + chunk : n;
+  const __half* x = X + static_cast<long long>(b) * n;
+  float s = 0.f;
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) && (n % 8 == 0);
+  if (vec) {
+    for (long long i = lo + threadIdx.x * 8LL; i < hi; i += 256LL * 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(x + i);
+      const __half2* hp = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(hp[j]);
+        s = fmaf(f.x, f.x, s);
+        s = fmaf(f.y, f.y, s);
+      }
+    }
+  } else {
+    for (long long i = lo + threadIdx.x; i < hi; i += 256) {
+      const float f = __half2float(x[i]);
+      s = fmaf(f, f, s);
+    }
+  }
+  s = warp_sum(s);
+  if (threadIdx.x % kWarp == 0) red[threadIdx.x / kWarp] = s;
+  __syncthreads();
+  if (threadIdx.x < kWarp) {
+    float v = threadIdx.x < 8 ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) parts[static_cast<size_t>(b) * nparts + p] = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a7: W[S_i] <- round_p(W[S_i] - lr O[i]).  One warp per selected row.
+// ---------------------------------------------------------------------------
+template <int PD, bool VEC>
+__global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ ScatterArgs a) {
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  if (gw >= total) return;
+  const int b = static_cast<int>(gw / a.k);
+  const int i = static_cast<int>(gw % a.k);
+  const int row = a.idx[static_cast<size_t>(b) * a.k + i];
+  if (row < 0 || row >= a.rows) {  // never expected: record and skip the access
+    if (lane == 0) atomicOr(a.status, kDevCheck);
+    return;
+  }
+  const __half* O = a.O + static_cast<long long>(b) * a.o_bstride + static_cast<size_t>(i) * a.ld_o;
+  const int cols = a.cols;
+  const float nlr = -a.lr;
+  if constexpr (PD == kBF16) {
+    __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(a.W[b]) + static_cast<size_t>(row) * cols;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < cols; c += kWarp * 8) {
+        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
+        const uint4 w = *reinterpret_cast<const uint4*>(W + c);
+        float wf[8];
+        bf16x8_to_f32(w, wf);
+        const __half2* oh = reinterpret_cast<const __half2*>(&o);
+        uint32_t outw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 of = __half22float2(oh[j]);
+          const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(nlr, of.x, wf[2 * j]), fmaf(nlr, of.y, wf[2 * j + 1]));
+          outw[j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
+        *reinterpret_cast<uint4*>(W + c) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      }
+    } else {
+      for (int c = lane; c < cols; c += kWarp)
+        W[c] = __float2bfloat16_rn(fmaf(nlr, __half2float(O[c]), __bfloat162float(W[c])));
+    }
+  } else {
+    float* W = reinterpret_cast<float*>(a.W[b]) + static_cast<size_t>(row) * cols;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < cols; c += kWarp * 8) {
+        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
+        const __half2* oh = reinterpret_cast<const __half2*>(&o);
+        float4 w0 = *reinterpret_cast<const float4*>(W + c);
+        float4 w1 = *reinterpret_cast<const float4*>(W + c + 4);
+        float2 o0 = __half22float2(oh[0]), o1 = __half22float2(oh[1]);
+        float2 o2 = __half22float2(oh[2]), o3 = __half22float2(oh[3]);
+        w0.x = fmaf(nlr, o0.x, w0.x); w0.y = fmaf(nlr, o0.y, w0.y);
+        w0.z = fmaf(nlr, o1.x, w0.z); w0.w = fmaf(nlr, o1.y, w0.w);
+        w1.x = fmaf(nlr, o2.x, w1.x); w1.y = fmaf(nlr, o2.y, w1.y);
+        w1.z = fmaf(nlr, o3.x, w1.z); w1.w = fmaf(nlr, o3.y, w1.w);
+        *reinterpret_cast<float4*>(W + c) = w0;
+        *reinterpret_cast<float4*>(W + c + 4) = w1;
+      }
+    } else {
+      for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, __half2float(O[c]), W[c]);
+    }
+  }
+}
+
+inline unsigned ceil_div(long long a, long long b) { return static_cast<unsigned>((a + b - 1) / b); }
+
+}  // namespace
+
+cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.batch) * a.rows;
+  const dim3 grid(ceil_div(total, 8)), block(256);
+  const bool has_grad = a.G[0] != nullptr;
+  if (vec) {
+    if (!has_grad) accum_rownorm_kernel<true, -1><<<grid, block, 0, s>>>(a);
+    else if (a.grad_dtype == kBF16) accum_rownorm_kernel<true, kBF16><<<grid, block, 0, s>>>(a);
+    else accum_rownorm_kernel<true, kF32><<<grid, block, 0, s>>>(a);
+  } else {
+    if (!has_grad) accum_rownorm_kernel<false, -1><<<grid, block, 0, s>>>(a);
+    else if (a.grad_dtype == kBF16) accum_rownorm_kernel<false, kBF16><<<grid, block, 0, s>>>(a);
+    else accum_rownorm_kernel<false, kF32><<<grid, block, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
+  topk_kernel<<<a.batch, kTopkThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
+  const dim3 grid(ceil_div(a.m, kGCols), ceil_div(a.k, kGRows), a.batch), block(256);
+  if (a.src_f32) {
+    if (vec) gather_kernel<true, true><<<grid, block, 0, s>>>(a);
+    else gather_kernel<true, false><<<grid, block, 0, s>>>(a);
+  } else {
+    if (vec) gather_kernel<false, true><<<grid, block, 0, s>>>(a);
+    else gather_kernel<false, false><<<grid, block, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts, int nparts,
+                             cudaStream_t s) {
+  sumsq_f16_kernel<<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  const dim3 grid(ceil_div(total, 8)), block(256);
+  if (a.param_dtype == kBF16) {
+    if (vec) scatter_kernel<kBF16, true><<<grid, block, 0, s>>>(a);
+    else scatter_kernel<kBF16, false><<<grid, block, 0, s>>>(a);
+  } else {
+    if (vec) scatter_kernel<kF32, true><<<grid, block, 0, s>>>(a);
+    else scatter_kernel<kF32, false><<<grid, block, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dion3
