@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the Dion3 optimizer step on GB300 (one rank per GPU).
+
+Default workload: the 7B-shaped matrix set (d = 4096, 32 layers: 128 x
+4096x4096, 64 x 4096x11008, 32 x 11008x4096; bf16 parameters and gradients,
+fp32 momentum) stepped at f = 1/4, as three shape groups in one dion3_step.
+A "step" is one full Dion3 optimizer step over every matrix of the set:
+momentum accumulation + l1 selection, gather/normalise, fp16 Gram
+Newton-Schulz (T = 5, restart at 3) and the row-scatter update.
+
+Printed (rank 0, one JSON line):
+  value        useful TFLOP/s of the whole job (Gram-NS FLOPs with a triangle
+               counted as half, summed over all ranks' matrices) / max-over-
+               ranks step time; inputs resident in HBM (65 GB, far above L2).
+  e2e          the same metric when every step also copies its gradients from
+               pinned host memory and reads the selected row indices back.
+  roofline     the dominant kernel of the timed region (CUDA events around each
+               launch, via the library's launch trace) against the measured
+               peak in MEASURED_PEAKS.json.
+  cpu_baseline the float64 CPU oracle timed on a bounded sample (one matrix of
+               each shape group) and scaled to the full set.
+
+--impl reference times the CPU oracle (the only reference this method has:
+there is no reference implementation to install) on the same workload and
+metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Dion3 optimizer-step ms & useful TFLOP/s (frac of GB300 FP16 peak) per model at f"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# Workload description
+# ---------------------------------------------------------------------------
+
+def workload_groups(name: str):
+    """[(rows, cols, batch, param_dtype, grad_dtype)] and a description."""
+    import workloads
+    if name in ("7b", "1b"):
+        spec = workloads.MODEL_SETS[name]
+        groups = [(r, c, b, "bf16", "bf16") for (r, c, b) in workloads.model_groups(name)]
+        desc = (f"{name.upper()}-shaped matrix set (d={spec['d']}, {spec['layers']} layers: "
+                + ", ".join(f"{b}x {r}x{c}" for (r, c, b, _, _) in groups) + ")")
+        return groups, desc
+    if name == "gapped":
+        return [(1024, 4096, 1, "bf16", "bf16")], "one 1024x4096 matrix (gapped l1 ladder)"
+    if name == "single":
+        return [(256, 1024, 1, "f32", "f32")], "one fp32 256x1024 matrix"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def useful_flops_total(groups, f, hp_kwargs, d3):
+    hp = d3.HParams(f=f, **hp_kwargs)
+    tot = 0.0
+    for (r, c, b, _, _) in groups:
+        k = d3.num_selected(f, r)
+        tot += b * d3.useful_flops(k, c, hp)
+    return tot
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM traffic per launch of `kernel` from a committed ncu summary, or None
+    if none exists or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    with open(src, "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != rec["source_sha256"]:
+            return None
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def build_state(groups, device, seed_base, d3):
+    """Per-group contiguous [batch, n, m] tensors; seeded Gaussian W and G,
+    zero momentum (the warm-up steps fill it)."""
+    import torch
+    import workloads
+    dt = {"bf16": torch.bfloat16, "f32": torch.float32}
+    state = []
+    for gi, (r, c, b, pd, gd) in enumerate(groups):
+        W = torch.empty((b, r, c), dtype=dt[pd], device=device)
+        G = torch.empty((b, r, c), dtype=dt[gd], device=device)
+        M = torch.zeros((b, r, c), dtype=torch.float32, device=device)
+        for i in range(b):
+            workloads.device_gaussian_(W[i], 0.02, seed_base + 100000 * gi + 2 * i)
+            workloads.device_gaussian_(G[i], 0.01, seed_base + 100000 * gi + 2 * i + 1)
+        state.append({"W": W, "G": G, "M": M, "rows": r, "cols": c, "batch": b,
+                      "group": d3.Group(params=list(W.unbind(0)), grads=list(G.unbind(0)),
+                                        momentum=list(M.unbind(0)))})
+    return state
+
+
+def cpu_baseline(state, groups, f, hp, flops_total):
+    """Time the float64 oracle on one matrix per shape group (the state as it is
+    now), scale by the group sizes."""
+    import numpy as np
+    from oracle import dion3_step as oracle_step
+    t_est = 0.0
+    parts = []
+    for st, (r, c, b, pd, gd) in zip(state, groups):
+        W = st["W"][0].float().cpu().numpy()
+        M = st["M"][0].cpu().numpy()
+        G = st["G"][0].float().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle_step(W, M, G, f=f, mu=hp.mu, lr=hp.lr, eps=hp.eps, param_dtype=pd)
+        dt = time.perf_counter() - t0
+        t_est += dt * b
+        parts.append(f"{r}x{c}: {dt:.2f} s x {b}")
+    ms = t_est * 1e3
+    return {"value": flops_total / (t_est * 1e12), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "ms_per_step_est": ms,
+            "sample": "float64 oracle on one matrix of each shape group, scaled by group size ("
+                      + "; ".join(parts) + ")"}
+
+
+def run_ours(args, rank, world, device_index):
+    import torch
+    import matrix_orthogonalizing_optimizer_shape_gb300 as d3
+
+    torch.cuda.set_device(device_index)
+    device = torch.device("cuda", device_index)
+    d3.load_library()
+    groups, desc = workload_groups(args.workload)
+    hp_kwargs = dict(mu=0.95, lr=0.02, eps=1e-7, ns_steps=5, restart_iter=3)
+    hp = d3.HParams(f=args.f, **hp_kwargs)
+    flops_rank = useful_flops_total(groups, args.f, hp_kwargs, d3)
+
+    state = build_state(groups, device, 7 + 1000003 * rank, d3)
+    cgroups = [s["group"] for s in state]
+    ws = d3.alloc_workspace(d3.workspace_size(cgroups, hp), device=device)
+    sel = [torch.empty((s["batch"], d3.num_selected(args.f, s["rows"])), dtype=torch.int32,
+                       device=device) for s in state]
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
+    d3.device_status(stream)
+
+    # Timed region: K steps, per-launch events through the library trace.
+    clocks = ClockSampler(device_index)
+    barrier()
+    torch.cuda.synchronize(device)
+    clocks.start()
+    d3.trace_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clock_info = clocks.stop()
+    trace = d3.trace_collect()
+    d3.trace_enable(False)
+    d3.device_status(stream)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    launches = sum(v["launches"] for v in trace.values())
+
+    # End to end: pinned host gradients -> device, step, selected rows -> host.
+    e2e = None
+    if not args.no_e2e:
+        host_g = [torch.empty(s["G"].shape, dtype=s["G"].dtype, pin_memory=True).copy_(s["G"])
+                  for s in state]
+        host_sel = [torch.empty(x.shape, dtype=torch.int32).pin_memory() for x in sel]
+        h2d = sum(h.numel() * h.element_size() for h in host_g)
+        d2h = sum(h.numel() * h.element_size() for h in host_sel)
+        barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for s, h in zip(state, host_g):
+                s["G"].copy_(h, non_blocking=True)
+            d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
+            for x, h in zip(sel, host_sel):
+                h.copy_(x, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+        ems = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * flops_rank / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del host_g
+
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    dom_name, dom = max(trace.items(), key=lambda kv: kv[1]["total_ms"])
+    if dom["useful_flops"] > 0:
+        achieved = dom["useful_flops"] / (dom["total_ms"] * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "peak_kind": f"bf16 sustained ({peak_src}); fp16 dense rate = bf16 dense rate"}
+    else:
+        achieved = dom["algo_bytes"] / (dom["total_ms"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "peak_kind": f"hbm copy ({peak_src})"}
+    roof["frac"] = achieved / peak
+    roof["kernel"] = dom_name
+    roof["launches_per_step"] = dom["launches"] / args.steps
+    tr = traffic_record(dom_name)
+    roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
+    kernels = {}
+    tot_ms = sum(v["total_ms"] for v in trace.values())
+    for name, v in sorted(trace.items(), key=lambda kv: -kv[1]["total_ms"]):
+        kv = {"launches_per_step": v["launches"] / args.steps,
+              "ms_per_step": v["total_ms"] / args.steps, "share": v["total_ms"] / tot_ms}
+        if v["useful_flops"] > 0:
+            kv["tflops"] = v["useful_flops"] / (v["total_ms"] * 1e-3) / 1e12
+        if v["algo_bytes"] > 0 and v["useful_flops"] == 0:
+            kv["gbs"] = v["algo_bytes"] / (v["total_ms"] * 1e-3) / 1e9
+        kernels[name] = kv
+
+    value = world * flops_rank / (ms_max * 1e-3) / 1e12
+    bf16_peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"{desc}, f={args.f}", "f": args.f,
+                   "matrices": sum(g[2] for g in groups), "params_per_gpu": sum(g[0] * g[1] * g[2] for g in groups),
+                   "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
+                   "ns": "Gram NS T=5 restart@3, fp16 operands, fp32 accumulate",
+                   "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
+                   "frac_of_fp16_peak": value / world / bf16_peak,
+                   "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
+                   "parallelism": f"{world} independent ranks (no collective on the data path)"},
+        "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+        "gpu_launches_per_step": launches / args.steps, "clocks": clock_info,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(state, groups, args.f, hp, flops_rank)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    import numpy as np
+    import workloads
+    from oracle import dion3_step as oracle_step, num_selected as o_num_selected
+
+    groups, desc = workload_groups(args.workload)
+    # Useful FLOPs of the Gram-NS schedule, counted with the oracle's own op log.
+    from oracle import gram_newton_schulz, gram_ns_useful_flops
+    log = []
+    gram_newton_schulz(np.ones((2, 3)) / 6.0, steps=5, restart_iter=3, op_log=log)
+    flops = 0.0
+    for (r, c, b, pd, gd) in groups:
+        k = o_num_selected(args.f, r)
+        s, L = min(k, c), max(k, c)
+        flops += b * gram_ns_useful_flops([(op[0], s, L) if op[0] != "sym" else ("sym", s)
+                                           for op in log])
+    samples = []
+    for (r, c, b, pd, gd) in groups:
+        samples.append({
+            "W": workloads.gaussian((r, c), 0.02, seed=1, dtype=pd),
+            "M": workloads.gaussian((r, c), 0.05, seed=2),
+            "G": workloads.gaussian((r, c), 0.01, seed=3, dtype=gd)})
+    # Each step runs the oracle on ONE matrix, rotating through the shape groups;
+    # the step's full-set estimate combines the latest per-matrix time of every
+    # group, scaled by the group sizes.  W >= 3 warm-up steps cover every group
+    # of the model-shaped sets before the timed steps.
+    group_t = [None] * len(groups)
+    times = []
+    for it in range(args.warmup + args.steps):
+        g = it % len(groups)
+        smp = samples[g]
+        r, c, b, pd, gd = groups[g]
+        t0 = time.perf_counter()
+        W, M, _, _ = oracle_step(smp["W"], smp["M"], smp["G"], f=args.f, mu=0.95, lr=0.02,
+                                 param_dtype=pd)
+        group_t[g] = time.perf_counter() - t0
+        smp["W"], smp["M"] = W.astype(np.float32), M
+        if it >= args.warmup:
+            times.append(sum(t * grp[2] for t, grp in zip(group_t, groups)))
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    sample = ("float64 oracle on one matrix per step, rotating through the shape groups; each "
+              "step's estimate sums the latest per-matrix time of every group times its size "
+              f"({', '.join(f'{r}x{c} x{b}' for (r, c, b, _, _) in groups)})")
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{desc}, f={args.f}", "f": args.f},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="7b", choices=["7b", "1b", "gapped", "single"])
+    ap.add_argument("--f", type=float, default=0.25)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -217,6 +217,28 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
                         int32_t* const* sel_idx_out, dion3_stream_t stream);
 
 /*
+ * Launch trace (measurement aid).  While enabled, every kernel launch made by
+ * this library is bracketed by two CUDA events on its stream and recorded with
+ * its algorithmic work: useful FLOPs for the tensor-core GEMM (a triangle
+ * counted as half) and bytes that must cross HBM for the memory-bound
+ * kernels.  dion3_trace_enable(1) starts a fresh record, dion3_trace_enable(0)
+ * stops and discards it.  dion3_trace_collect() waits for the recorded events,
+ * aggregates them per kernel into out[0 .. min(*count, capacity)), sets *count
+ * to the number of kernels seen and clears the record (recording goes on if
+ * enabled).  Host-side cost: two cudaEventRecord calls per launch.
+ */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+  double useful_flops;
+  double algo_bytes;
+} dion3_trace_entry;
+
+dion3_status dion3_trace_enable(int32_t on);
+dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32_t* count);
+
+/*
  * Synchronises `stream`, reads and clears the device status word written by
  * bounded device-side waits, and returns DION3_OK, DION3_ERR_TIMEOUT or
  * DION3_ERR_DEVICE_CHECK (or DION3_ERR_CUDA if synchronisation fails).

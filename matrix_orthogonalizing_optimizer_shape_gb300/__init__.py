@@ -37,7 +37,8 @@ EXPORTED = (
     "dion3_abi_version", "dion3_status_string", "dion3_last_error", "dion3_num_selected",
     "dion3_useful_flops", "dion3_select_workspace_size", "dion3_select_rows",
     "dion3_gram_ns_workspace_size", "dion3_gram_ns_batched", "dion3_workspace_size",
-    "dion3_step", "dion3_device_status", "dion3_gemm_f16",
+    "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
+    "dion3_trace_collect",
 )
 
 
@@ -64,6 +65,12 @@ class _Group(ctypes.Structure):
                 ("momentum", ctypes.POINTER(ctypes.c_void_p))]
 
 
+class _TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double), ("useful_flops", ctypes.c_double),
+                ("algo_bytes", ctypes.c_double)]
+
+
 _vp, _sz, _i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
 _SIGS = {
     "dion3_abi_version": (ctypes.c_size_t, []),
@@ -88,6 +95,8 @@ _SIGS = {
                                       _vp, _i32, ctypes.c_int64, _vp, _i32, ctypes.c_int64,
                                       _vp, _i32, ctypes.c_int64,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp]),
+    "dion3_trace_enable": (ctypes.c_int, [_i32]),
+    "dion3_trace_collect": (ctypes.c_int, [ctypes.POINTER(_TraceEntry), _i32, ctypes.POINTER(_i32)]),
 }
 
 _LIB = None
@@ -286,6 +295,28 @@ def gemm_f16(A, B, D=None, DT=None, C=None, *, mode: int = GEMM_RECT, alpha: flo
     a, b, c, d, dt = geom(A), geom(B), geom(C), geom(D), geom(DT)
     _check(load_library().dion3_gemm_f16(mode, M, N, K, batch, *a, *b, *c, *d, *dt,
                                          alpha, beta, gamma, _stream(stream)))
+
+
+def trace_enable(on: bool = True):
+    """Start (or stop) recording per-launch CUDA events (see dion3_trace_enable)."""
+    _check(load_library().dion3_trace_enable(1 if on else 0))
+
+
+def trace_collect() -> dict:
+    """{kernel: {launches, total_ms, useful_flops, algo_bytes}} since the last
+    collect; waits for the recorded events."""
+    lib = load_library()
+    cap = 32
+    buf = (_TraceEntry * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib.dion3_trace_collect(buf, cap, ctypes.byref(n)))
+    out = {}
+    for i in range(min(n.value, cap)):
+        e = buf[i]
+        out[e.name.decode()] = {"launches": int(e.launches), "total_ms": float(e.total_ms),
+                                "useful_flops": float(e.useful_flops),
+                                "algo_bytes": float(e.algo_bytes)}
+    return out
 
 
 def device_status(stream=None):

@@ -59,6 +59,56 @@ dion3_status ok() {
   return DION3_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Optional launch trace: when enabled, every kernel launch is bracketed by two
+// CUDA events on its stream and recorded with its algorithmic work (useful
+// FLOPs for the GEMM, bytes for the memory-bound kernels).
+// ---------------------------------------------------------------------------
+struct TraceRec {
+  const char* name;
+  cudaEvent_t a, b;
+  double flops, bytes;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void trace_clear_locked() {
+  for (auto& r : g_trace) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_trace.clear();
+}
+
+template <class Launch>
+cudaError_t traced(const char* name, double flops, double bytes, cudaStream_t s, Launch&& launch) {
+  std::unique_lock<std::mutex> lock(g_trace_mu);
+  if (!g_trace_on) {
+    lock.unlock();
+    return launch();
+  }
+  cudaEvent_t a = pooled_event(), b = pooled_event();
+  if (a == nullptr || b == nullptr) return cudaErrorMemoryAllocation;
+  cudaEventRecord(a, s);
+  const cudaError_t e = launch();
+  cudaEventRecord(b, s);
+  g_trace.push_back({name, a, b, flops, bytes});
+  return e;
+}
+
 inline long long round_up(long long x, long long a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -156,6 +206,38 @@ void gather_targets(const NsPlan& p, GatherArgs& g) {
   }
 }
 
+// Traced launch helpers: the algorithmic work of one launch.
+cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
+  const double flops = g.mode == kSymLower ? static_cast<double>(g.M) * g.M * g.K * g.batch
+                                           : 2.0 * g.M * g.N * g.K * g.batch;
+  const double bytes = 2.0 * g.batch * (static_cast<double>(g.M) * g.K + static_cast<double>(g.N) * g.K);
+  return traced("gemm_tcgen05", flops, bytes, s, [&] { return launch_gemm(g, st, s); });
+}
+cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
+  const double gb = a.G[0] == nullptr ? 0.0 : (a.grad_dtype == kBF16 ? 2.0 : 4.0);
+  const double wb = a.G[0] == nullptr ? 0.0 : 4.0;
+  const double bytes = static_cast<double>(a.batch) * a.rows * (a.cols * (4.0 + gb + wb) + 8.0);
+  return traced("accum_rownorm", 0.0, bytes, s, [&] { return launch_accum_rownorm(a, vec, s); });
+}
+cudaError_t traced_topk(const TopkArgs& t, cudaStream_t s) {
+  const double bytes = static_cast<double>(t.batch) * (t.rows * 8.0 + t.k * 4.0 + 4.0);
+  return traced("topk_select", 0.0, bytes, s, [&] { return launch_topk(t, s); });
+}
+cudaError_t traced_gather(const GatherArgs& g, bool vec, cudaStream_t s) {
+  const double per = g.src_f32 ? (4.0 + (g.decay ? 4.0 : 0.0)) : 2.0;
+  const double bytes = static_cast<double>(g.batch) * g.k * g.m * (per + 4.0);
+  return traced("gather_normalize", 0.0, bytes, s, [&] { return launch_gather(g, vec, s); });
+}
+cudaError_t traced_sumsq(const __half* X, long long n, int batch, float* parts, int nparts, cudaStream_t s) {
+  return traced("sumsq_f16", 0.0, 2.0 * n * batch, s,
+                [&] { return launch_sumsq_f16(X, n, batch, parts, nparts, s); });
+}
+cudaError_t traced_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
+  const double pb = a.param_dtype == kBF16 ? 2.0 : 4.0;
+  const double bytes = static_cast<double>(a.batch) * a.k * a.cols * (2.0 + 2.0 * pb);
+  return traced("scatter_update", 0.0, bytes, s, [&] { return launch_scatter(a, vec, s); });
+}
+
 // Useful FLOPs of the schedule run_gram_ns() launches (triangle = half).
 double schedule_flops(int k, int m, const dion3_hparams& hp) {
   const double s = std::min(k, m), L = std::max(k, m);
@@ -208,7 +290,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   auto launch = [&](const GemmDesc& g) -> dion3_status {
     const char* why = nullptr;
     if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
-    const cudaError_t e = launch_gemm(g, st, stream);
+    const cudaError_t e = traced_gemm(g, st, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
     return DION3_OK;
   };
@@ -405,12 +487,12 @@ dion3_status dion3_select_rows(int32_t rows, int32_t cols, int32_t batch, float*
     }
     a.l1 = l1 + static_cast<size_t>(b0) * rows;
     a.sq = sq + static_cast<size_t>(b0) * rows;
-    const cudaError_t e = launch_accum_rownorm(a, vec, s);
+    const cudaError_t e = traced_accum(a, vec, s);
     if (e != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
   }
   TopkArgs t{};
   t.rows = rows; t.k = k; t.batch = batch; t.l1 = l1; t.sq = sq; t.idx = idx_out; t.fro2 = fro2_out;
-  const cudaError_t e = launch_topk(t, s);
+  const cudaError_t e = traced_topk(t, s);
   if (e != cudaSuccess) return cuda_fail(e, "topk launch");
   return ok();
 }
@@ -449,7 +531,7 @@ dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const vo
   constexpr int kParts = 64;
   float* parts = c.take<float>(static_cast<long long>(batch) * kParts);
   const long long n = static_cast<long long>(k) * m;
-  cudaError_t e = launch_sumsq_f16(static_cast<const __half*>(X), n, batch, parts, kParts, s);
+  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, s);
   if (e != cudaSuccess) return cuda_fail(e, "sumsq launch");
   GatherArgs g{};
   g.k = k; g.m = m; g.batch = batch; g.src_f32 = false;
@@ -457,7 +539,7 @@ dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const vo
   g.fro2 = parts; g.fro2_parts = kParts; g.eps = hp->eps; g.decay = false;
   g.n = k; g.status = st;
   gather_targets(p, g);
-  e = launch_gather(g, m % 4 == 0, s);
+  e = traced_gather(g, m % 4 == 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   NsOut out{static_cast<__half*>(O), static_cast<long long>(k) * m, m};
   if ((rc = run_gram_ns(p, *hp, out, st, s)) != DION3_OK) return rc;
@@ -518,11 +600,11 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       }
       a.l1 = gp.l1 + static_cast<size_t>(b0) * g.rows;
       a.sq = gp.sq + static_cast<size_t>(b0) * g.rows;
-      if ((e = launch_accum_rownorm(a, vec, s)) != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
+      if ((e = traced_accum(a, vec, s)) != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
     }
     TopkArgs t{};
     t.rows = g.rows; t.k = gp.k; t.batch = g.batch; t.l1 = gp.l1; t.sq = gp.sq; t.idx = idx; t.fro2 = gp.fro2;
-    if ((e = launch_topk(t, s)) != cudaSuccess) return cuda_fail(e, "topk launch");
+    if ((e = traced_topk(t, s)) != cudaSuccess) return cuda_fail(e, "topk launch");
     // (b) gather/normalise (+ decay of the selected momentum rows), Gram-NS.
     for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
       const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
@@ -535,7 +617,7 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       gather_targets(gp.ns, ga);
       ga.out_rows += ga.rows_bstride * b0;
       ga.out_cols += ga.cols_bstride * b0;
-      if ((e = launch_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
+      if ((e = traced_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
     }
     NsOut out{gp.O, gp.o_bs, gp.ld_o};
     if ((rc = run_gram_ns(gp.ns, *hp, out, st, s)) != DION3_OK) return rc;
@@ -549,7 +631,7 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       sa.O = gp.O + gp.o_bs * b0; sa.o_bstride = gp.o_bs; sa.ld_o = gp.ld_o;
       sa.lr = lr_eff;
       sa.status = st;
-      if ((e = launch_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
+      if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
   }
   return ok();
@@ -587,8 +669,44 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
   if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
   unsigned* st = device_status_ptr();
   if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
-  const cudaError_t e = launch_gemm(g, st, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = traced_gemm(g, st, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+  return ok();
+}
+
+dion3_status dion3_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  trace_clear_locked();
+  g_trace_on = on != 0;
+  return ok();
+}
+
+dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32_t* count) {
+  if (count == nullptr || (out == nullptr && capacity > 0) || capacity < 0)
+    return fail(DION3_ERR_INVALID_ARG, "count must not be NULL and out must hold capacity entries");
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  std::vector<dion3_trace_entry> agg;
+  for (const auto& r : g_trace) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event synchronise");
+    float ms = 0.f;
+    if ((e = cudaEventElapsedTime(&ms, r.a, r.b)) != cudaSuccess) return cuda_fail(e, "trace elapsed time");
+    dion3_trace_entry* slot = nullptr;
+    for (auto& x : agg)
+      if (strncmp(x.name, r.name, sizeof x.name) == 0) slot = &x;
+    if (slot == nullptr) {
+      agg.push_back(dion3_trace_entry{});
+      slot = &agg.back();
+      snprintf(slot->name, sizeof slot->name, "%s", r.name);
+    }
+    slot->launches += 1;
+    slot->total_ms += ms;
+    slot->useful_flops += r.flops;
+    slot->algo_bytes += r.bytes;
+  }
+  *count = static_cast<int32_t>(agg.size());
+  for (int i = 0; i < static_cast<int>(agg.size()) && i < capacity; ++i) out[i] = agg[i];
+  trace_clear_locked();
   return ok();
 }
 
