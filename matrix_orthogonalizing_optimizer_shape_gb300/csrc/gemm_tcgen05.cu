@@ -3,11 +3,11 @@
 // D = A B^T with A [batch][M][K] and B [batch][N][K] in fp16, both K-major,
 // fp32 accumulation in tensor memory, and the epilogue
 //     v = alpha D + beta C + gamma I
-// rounded to fp16.  In kSymLower mode only the lower-triangle tiles of the
-// (symmetric) M x M result are computed; each tile is written in place and
-// mirrored into the upper triangle, so the stored matrix is exactly
-// symmetric.  In kRect mode every tile is computed and written in the normal
-// and/or the transposed orientation.
+// rounded to fp16.  In kSymLower mode (M == N, symmetric result) only tiles
+// that meet the lower triangle are computed; every element on or below the
+// diagonal is written in place and mirrored above it, so the stored matrix is
+// exactly symmetric.  In kRect mode every tile is computed and written in the
+// normal and/or the transposed orientation.
 //
 // Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of the
 // paper).  First-level paragraph: Newton-Schulz iterates on the small
@@ -19,21 +19,26 @@
 //   Q <- Z Q, T = R Z, R <- Z T  (B symmetric, so B^T = B; kSymLower)
 //   Y_new^T = Y^T Q, O = (Y^T Q)^T  (A = Y^T, B = Q, kRect)
 //
-// Data path per CTA (one 128 x BN output tile, 4 warps):
-//   warp 0 lane 0: TMA producer, 128-byte-swizzled 64-wide K slabs of A and B
-//                  into a STAGES-deep shared-memory ring (mbarrier expect_tx);
-//   warp 1 lane 0: issues tcgen05.mma (cta_group::1, kind::f16, M=128, N=BN,
-//                  K=16) into a BN-column TMEM accumulator; tcgen05.commit
-//                  frees each ring slot and finally signals the epilogue;
-//   all 4 warps:   tcgen05.ld 32 lanes x 32 columns per warp, epilogue, stores.
-// Every mbarrier wait is bounded (about one second, %globaltimer); a wait that
-// runs out sets a bit in the device status word and the CTA winds down (the
-// TMEM it holds is freed on every path).
+// Kernel: persistent (one CTA per SM, tiles handed out round-robin over the
+// whole batch), 128 x 256 output tiles, 6 warps with fixed roles:
+//   warp 0 lane 0  TMA producer: 128-byte-swizzled 64-wide K slabs of A (128
+//                  rows) and B (256 rows) into a 4-deep shared-memory ring;
+//   warp 1         allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//                  (cta_group::1, kind::f16, M = 128, N = 256, K = 16) into one
+//                  of two 256-column fp32 accumulators, so the epilogue of a
+//                  tile overlaps the main loop of the next;
+//   warps 2..5     epilogue: tcgen05.ld of the 32 TMEM lanes each warp may
+//                  access (warp % 4), alpha/beta/gamma, fp16 stores.
+// Every mbarrier wait is bounded (about one second of %globaltimer); a wait
+// that runs out sets a bit in the device status word and the CTA winds down:
+// the producer waits (bounded) for its copies in flight, the MMA issuer for
+// its MMAs, and the TMEM is freed on every path.
 #include "internal.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace dion3 {
@@ -41,11 +46,16 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // fp16 elements per 128-byte swizzle row
-constexpr int kThreads = 128;
+constexpr int BN = 256;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 struct GemmParams {
-  int M, N, K, mode, tiles_n;
+  int M, N, K, mode;
+  int tiles_r, tiles_c;      // row (128) and column (256) tile counts of one matrix
+  int tiles_per_mat, total_tiles;
   float alpha, beta, gamma;
   const __half* C; long long c_bs; int ldc;
   __half* out; long long out_bs; int ld_out;
@@ -176,209 +186,258 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
 // M >> 4 in bits 24-28.
-template <int N>
 __device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-// Lower-triangle tile t -> (i, j), i >= j, t = i (i + 1) / 2 + j.
-__device__ __forceinline__ void tri_tile(int t, int& i, int& j) {
-  int r = static_cast<int>((sqrtf(8.0f * static_cast<float>(t) + 1.0f) - 1.0f) * 0.5f);
-  while ((r + 1) * (r + 2) / 2 <= t) ++r;
-  while (r * (r + 1) / 2 > t) --r;
-  i = r;
-  j = t - r * (r + 1) / 2;
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int BN, int STAGES>
-struct Layout {
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+// Tile t of one matrix -> (row tile bi, column tile bc).  kSymLower keeps
+// the tiles that meet the lower triangle: 128 bi + 127 >= 256 bc, i.e.
+// bi >= 2 bc, enumerated column by column.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& bi, int& bc) {
+  if (p.mode == kSymLower) {
+    bc = 0;
+    for (;;) {
+      const int cnt = p.tiles_r - 2 * bc;
+      if (t < cnt) break;
+      t -= cnt;
+      ++bc;
+    }
+    bi = 2 * bc + t;
+  } else {
+    bi = t / p.tiles_c;
+    bc = t % p.tiles_c;
+  }
+}
+
+struct Smem {
+  static constexpr int kABytes = BM * BK * 2;   // 16 KB
+  static constexpr int kBBytes = BN * BK * 2;   // 32 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kRingBytes = STAGES * kStageBytes;
-  static constexpr int kBarBytes = (2 * STAGES + 1) * 8;
-  static constexpr int kDynSmem = 1024 /*alignment slack*/ + kRingBytes + kBarBytes + 16;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int kBarBytes = (2 * kStages + 5) * 8;
+  static constexpr int kDyn = 1024 + kRingBytes + kBarBytes + 16;
 };
 
-template <int BN, int STAGES>
+// Epilogue of one 32-row x 32-column chunk held by a warp: thread `lane` owns
+// row r; v[j] is column c0 + j of the fp32 accumulator.
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int bidx, int r, int c0, int row0,
+                                               const uint32_t (&v)[32]) {
+  if (r >= p.M) return;
+  const bool sym = p.mode == kSymLower;
+  const bool full = (c0 + 32 <= p.N);
+  float f[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
+  if (p.C != nullptr) {
+    const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
+    if (full && (p.ldc % 8 == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(crow + 8 * q);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __half22float2(h2[e]);
+          f[8 * q + 2 * e] = fmaf(p.beta, x.x, f[8 * q + 2 * e]);
+          f[8 * q + 2 * e + 1] = fmaf(p.beta, x.y, f[8 * q + 2 * e + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < p.N) f[j] = fmaf(p.beta, __half2float(crow[j]), f[j]);
+    }
+  }
+  if (p.gamma != 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (r == c0 + j) f[j] += p.gamma;
+  }
+  uint32_t hp[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const __half2 t = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+    hp[j] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  // In symmetric mode an element is kept when r >= c (written) and mirrored
+  // when r > c.  `below`: every element of this warp's chunk is strictly below
+  // the diagonal (row0 is the warp's first row).
+  const bool below = !sym || (row0 > c0 + 31);
+  __half* outb = p.out ? p.out + static_cast<long long>(bidx) * p.out_bs : nullptr;
+  if (outb != nullptr) {
+    __half* dst = outb + static_cast<size_t>(r) * p.ld_out + c0;
+    if (below && full && (p.ld_out % 8 == 0)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < p.N && (!sym || r >= c0 + j))
+          dst[j] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+    }
+  }
+  __half* tb = sym ? outb : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
+  if (tb != nullptr) {
+    const int ldt = sym ? p.ld_out : p.ld_outT;
+    // For a fixed column the warp's 32 lanes write 32 consecutive elements.
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int c = c0 + j;
+      if (c < p.N && (!sym || r > c))
+        tb[static_cast<size_t>(c) * ldt + r] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
-  using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
-  const uint32_t sB = base + STAGES * L::kABytes;
-  const uint32_t bar_full = base + L::kRingBytes;
-  const uint32_t bar_empty = bar_full + STAGES * 8;
-  const uint32_t bar_acc = bar_empty + STAGES * 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kRingBytes + L::kBarBytes);
+  const uint32_t sB = base + kStages * Smem::kABytes;
+  const uint32_t bar_full = base + Smem::kRingBytes;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+  const uint32_t bar_tfull = bar_empty + kStages * 8;
+  const uint32_t bar_tempty = bar_tfull + 2 * 8;
+  const uint32_t bar_drain = bar_tempty + 2 * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kBarBytes);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bidx = blockIdx.y;
-  int tm, tn;
-  if (p.mode == kSymLower) {
-    tri_tile(blockIdx.x, tm, tn);
-  } else {
-    tm = blockIdx.x / p.tiles_n;
-    tn = blockIdx.x % p.tiles_n;
-  }
-  const int m0 = tm * BM, n0 = tn * BN;
+  const int nkb = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_acc, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 128);
+    }
+    mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), BN);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nkb = (p.K + BK - 1) / BK;
 
-  if (warp == 0 && lane == 0) {
-    // TMA producer.
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
-      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, p.status)) break;
-      mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
-      tma_load_3d(sA + s * L::kABytes, &tmA, bar_full + 8 * s, kb * BK, m0, bidx);
-      tma_load_3d(sB + s * L::kBBytes, &tmB, bar_full + 8 * s, kb * BK, n0, bidx);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer.
-    constexpr uint32_t idesc = idesc_f16_f32<BN>();
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
-      if (!mbar_wait(bar_full + 8 * s, ph, p.status)) break;
-      tc_fence_after();
-      const uint64_t da = sdesc_kmajor_sw128(sA + s * L::kABytes);
-      const uint64_t db = sdesc_kmajor_sw128(sB + s * L::kBBytes);
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        // +32 bytes along K inside the swizzle row = +2 in the address field.
-        mma_f16_ss(tmem, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(bar_empty + 8 * s);
-    }
-    mma_commit(bar_acc);
-  }
-  __syncwarp();
-
-  // Epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w + 31.
-  // Warp-uniform outcome, so the .sync.aligned TMEM loads below never run in a
-  // partially active warp.
-  const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0u, p.status));
-  tc_fence_after();
-  if (acc_ok) {
-    const int r = m0 + warp * 32 + lane;
-    const bool sym = p.mode == kSymLower;
-    const bool diag = sym && (tm == tn);
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    __half* outb = p.out ? p.out + static_cast<long long>(bidx) * p.out_bs : nullptr;
-    __half* tb = sym ? outb : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
-    const int ldt = sym ? p.ld_out : p.ld_outT;
-    const __half* cb = p.C ? p.C + static_cast<long long>(bidx) * p.c_bs : nullptr;
-    for (int cc = 0; cc < BN; cc += 32) {
-      if (n0 + cc >= p.N) break;  // uniform across the CTA
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(trow + static_cast<uint32_t>(cc), v);
-      tmem_ld_wait();
-      if (r >= p.M) continue;
-      const int c0 = n0 + cc;
-      const bool full = (c0 + 32 <= p.N);
-      float f[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
-      if (cb != nullptr) {
-        const __half* crow = cb + static_cast<size_t>(r) * p.ldc + c0;
-        if (full && (p.ldc % 8 == 0)) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 u = *reinterpret_cast<const uint4*>(crow + 8 * q);
-            const __half2* h2 = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 x = __half22float2(h2[e]);
-              f[8 * q + 2 * e] = fmaf(p.beta, x.x, f[8 * q + 2 * e]);
-              f[8 * q + 2 * e + 1] = fmaf(p.beta, x.y, f[8 * q + 2 * e + 1]);
-            }
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const int bidx = t / p.tiles_per_mat;
+        int bi, bc;
+        tile_coords(p, t % p.tiles_per_mat, bi, bc);
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, p.status)) {
+            ok = false;
+            break;
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < p.N) f[j] = fmaf(p.beta, __half2float(crow[j]), f[j]);
+          mbar_arrive_expect_tx(bar_full + 8 * s, Smem::kStageBytes);
+          tma_load_3d(sA + s * Smem::kABytes, &tmA, bar_full + 8 * s, kb * BK, bi * BM, bidx);
+          tma_load_3d(sB + s * Smem::kBBytes, &tmB, bar_full + 8 * s, kb * BK, bc * BN, bidx);
         }
       }
-      if (p.gamma != 0.0f) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (r == c0 + j) f[j] += p.gamma;
+      // Wait (bounded) until every copy issued into the ring has landed, so no
+      // copy is in flight when the CTA exits.
+      for (uint32_t i = 0; i < kStages && i < kc; ++i) {
+        const uint32_t last = kc - 1 - i;  // most recent fill of stage last % kStages
+        mbar_wait(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
       }
-      uint32_t hp[16];  // 32 fp16 values, two per word
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_f16_f32();
+      uint32_t kc = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++tc) {
+        const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
+          if (!mbar_wait(bar_full + 8 * s, ph, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = sdesc_kmajor_sw128(sA + s * Smem::kABytes);
+          const uint64_t db = sdesc_kmajor_sw128(sB + s * Smem::kBBytes);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const __half2 t = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
-        hp[j] = *reinterpret_cast<const uint32_t*>(&t);
-      }
-
-      if (outb != nullptr) {
-        __half* dst = outb + static_cast<size_t>(r) * p.ld_out + c0;
-        if (!diag && full && (p.ld_out % 8 == 0)) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < p.N && (!diag || r >= c0 + j))
-              dst[j] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16_ss(d, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * s);
         }
+        mma_commit(bar_tfull + 8 * acc);
       }
-      if (tb != nullptr) {
-        // Mirror (symmetric) or transposed write: for a fixed column the warp's
-        // 32 lanes write 32 consecutive elements of one output row.
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int c = c0 + j;
-          if (c < p.N && (!diag || r > c))
-            tb[static_cast<size_t>(c) * ldt + r] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
-        }
+      // All MMAs issued by this thread complete before TMEM is freed.
+      mma_commit(bar_drain);
+      mbar_wait(bar_drain, 0u, p.status);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
+      const int bidx = t / p.tiles_per_mat;
+      int bi, bc;
+      tile_coords(p, t % p.tiles_per_mat, bi, bc);
+      const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int row0 = bi * BM + quad * 32;
+      const int r = row0 + lane;
+      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      for (int cc = 0; cc < BN; cc += 32) {
+        const int c0 = bc * BN + cc;
+        if (c0 >= p.N) break;  // uniform across the CTA
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
+        tmem_ld_wait();
+        epilogue_chunk(p, bidx, r, c0, row0, v);
       }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-constexpr int kBN = 128;
-constexpr int kStages = 4;
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
-    void* p = nullptr;
+    void* q_fn = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q_fn, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(q_fn);
   });
   return fn;
 }
@@ -398,6 +457,18 @@ bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, in
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cached[dev & 63] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev & 63] = n > 0 ? n : 1;
+  }
+  return cached[dev & 63];
 }
 
 }  // namespace
@@ -421,29 +492,37 @@ bool gemm_check(const GemmDesc& g, const char** why) {
 }
 
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
-  using L = Layout<kBN, kStages>;
-  auto kern = gemm_tcgen05_kernel<kBN, kStages>;
+  auto kern = gemm_tcgen05_kernel;
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
   });
   if (attr_err != cudaSuccess) return attr_err;
 
   CUtensorMap ta, tb;
   if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, kBN)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN)) return cudaErrorInvalidValue;
 
   GemmParams p{};
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
   p.mode = g.mode;
-  const int tiles_m = (g.M + BM - 1) / BM;
-  const int tiles_n = (g.N + kBN - 1) / kBN;
-  p.tiles_n = tiles_n;
+  p.tiles_r = (g.M + BM - 1) / BM;
+  p.tiles_c = (g.N + BN - 1) / BN;
+  if (g.mode == kSymLower) {
+    long long cnt = 0;
+    for (int bc = 0; 2 * bc < p.tiles_r; ++bc) cnt += p.tiles_r - 2 * bc;
+    p.tiles_per_mat = static_cast<int>(cnt);
+  } else {
+    p.tiles_per_mat = p.tiles_r * p.tiles_c;
+  }
+  const long long total = static_cast<long long>(p.tiles_per_mat) * g.batch;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.total_tiles = static_cast<int>(total);
   p.alpha = g.alpha;
   p.beta = g.beta;
   p.gamma = g.gamma;
@@ -458,15 +537,8 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.ld_outT = g.ld_outT;
   p.status = dev_status;
 
-  long long ntiles;
-  if (g.mode == kSymLower) {
-    // BM == kBN, so the tile grid is square.
-    ntiles = static_cast<long long>(tiles_m) * (tiles_m + 1) / 2;
-  } else {
-    ntiles = static_cast<long long>(tiles_m) * tiles_n;
-  }
-  if (ntiles > 0x7fffffffLL || g.batch > 65535) return cudaErrorInvalidConfiguration;
-  kern<<<dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(g.batch)), kThreads, L::kDynSmem, s>>>(ta, tb, p);
+  const int grid = static_cast<int>(std::min<long long>(total, sm_count()));
+  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
