@@ -48,12 +48,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Workload description
 # ---------------------------------------------------------------------------
 
-def workload_groups(name: str):
-    """[(rows, cols, batch, param_dtype, grad_dtype)] and a description."""
+def workload_groups(name: str, max_batch: int = 0):
+    """[(rows, cols, batch, param_dtype, grad_dtype)] and a description.
+    ``max_batch`` > 0 caps each group's matrix count (a small case of the same
+    shapes, for profiler captures)."""
     import workloads
     if name in ("7b", "1b"):
         spec = workloads.MODEL_SETS[name]
-        groups = [(r, c, b, "bf16", "bf16") for (r, c, b) in workloads.model_groups(name)]
+        groups = [(r, c, min(b, max_batch) if max_batch > 0 else b, "bf16", "bf16")
+                  for (r, c, b) in workloads.model_groups(name)]
         desc = (f"{name.upper()}-shaped matrix set (d={spec['d']}, {spec['layers']} layers: "
                 + ", ".join(f"{b}x {r}x{c}" for (r, c, b, _, _) in groups) + ")")
         return groups, desc
@@ -201,7 +204,7 @@ def run_ours(args, rank, world, device_index):
     torch.cuda.set_device(device_index)
     device = torch.device("cuda", device_index)
     d3.load_library()
-    groups, desc = workload_groups(args.workload)
+    groups, desc = workload_groups(args.workload, args.max_batch)
     hp_kwargs = dict(mu=0.95, lr=0.02, eps=1e-7, ns_steps=5, restart_iter=3)
     hp = d3.HParams(f=args.f, **hp_kwargs)
     flops_rank = useful_flops_total(groups, args.f, hp_kwargs, d3)
@@ -341,7 +344,7 @@ def run_reference(args):
     import workloads
     from oracle import dion3_step as oracle_step, num_selected as o_num_selected
 
-    groups, desc = workload_groups(args.workload)
+    groups, desc = workload_groups(args.workload, args.max_batch)
     # Useful FLOPs of the Gram-NS schedule, counted with the oracle's own op log.
     from oracle import gram_newton_schulz, gram_ns_useful_flops
     log = []
@@ -399,6 +402,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="7b", choices=["7b", "1b", "gapped", "single"])
     ap.add_argument("--f", type=float, default=0.25)
+    ap.add_argument("--max-batch", type=int, default=0,
+                    help="cap the matrices per shape group (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -207,11 +207,20 @@ void gather_targets(const NsPlan& p, GatherArgs& g) {
 }
 
 // Traced launch helpers: the algorithmic work of one launch.
+// With DION3_TRACE_DETAIL=1 in the environment the GEMM launches are
+// labelled by role (SYRK, symmetric square product, rectangular) instead of
+// under the kernel's name.
 cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
   const double flops = g.mode == kSymLower ? static_cast<double>(g.M) * g.M * g.K * g.batch
                                            : 2.0 * g.M * g.N * g.K * g.batch;
   const double bytes = 2.0 * g.batch * (static_cast<double>(g.M) * g.K + static_cast<double>(g.N) * g.K);
-  return traced("gemm_tcgen05", flops, bytes, s, [&] { return launch_gemm(g, st, s); });
+  static const bool detail = [] {
+    const char* v = getenv("DION3_TRACE_DETAIL");
+    return v != nullptr && v[0] == '1';
+  }();
+  const char* name = "gemm_tcgen05";
+  if (detail) name = g.mode == kRect ? "gemm_tcgen05:rect" : (g.K == g.M ? "gemm_tcgen05:sym_square" : "gemm_tcgen05:syrk");
+  return traced(name, flops, bytes, s, [&] { return launch_gemm(g, st, s); });
 }
 cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
   const double gb = a.G[0] == nullptr ? 0.0 : (a.grad_dtype == kBF16 ? 2.0 : 4.0);
