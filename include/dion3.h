@@ -217,6 +217,29 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
                         int32_t* const* sel_idx_out, dion3_stream_t stream);
 
 /*
+ * dion3_select_rows without a workspace, for callers that may not allocate
+ * device memory when they step the optimizer (their memory pool belongs to a
+ * host framework that must not be bypassed, their device-memory budget is
+ * fixed in advance, or they bind the C ABI without an allocator of their own).
+ * The paper has no counterpart: this is an interface convenience.
+ *
+ * Same arguments and results as dion3_select_rows minus ws / ws_bytes.  The
+ * row-norm scratch is a static device array inside the library (8 MiB, held by
+ * every GPU that loads the library until the process exits), so batch * rows
+ * must not exceed 1048576; larger requests return DION3_ERR_INVALID_ARG and
+ * enqueue nothing.  No cudaMalloc, cudaFree or other allocating call is made.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture begins.
+ * Every call on a device shares the array and leaves its contents behind
+ * (nothing in it needs to start at zero); calls whose work overlaps on the GPU
+ * race on it, so order them on one stream.
+ */
+dion3_status dion3_select_rows_noalloc(int32_t rows, int32_t cols, int32_t batch,
+                                       float* const* momentum, const void* const* grads,
+                                       int32_t grad_dtype, int32_t k, int32_t* idx_out,
+                                       float* fro2_out, dion3_stream_t stream);
+
+/*
  * Launch trace (measurement aid).  While enabled, every kernel launch made by
  * this library is bracketed by two CUDA events on its stream and recorded with
  * its algorithmic work: useful FLOPs for the tensor-core GEMM (a triangle

@@ -38,7 +38,7 @@ EXPORTED = (
     "dion3_useful_flops", "dion3_select_workspace_size", "dion3_select_rows",
     "dion3_gram_ns_workspace_size", "dion3_gram_ns_batched", "dion3_workspace_size",
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
-    "dion3_trace_collect",
+    "dion3_trace_collect", "dion3_select_rows_noalloc",
 )
 
 
@@ -96,6 +96,8 @@ _SIGS = {
                                       _vp, _i32, ctypes.c_int64,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp]),
     "dion3_trace_enable": (ctypes.c_int, [_i32]),
+    "dion3_select_rows_noalloc": (ctypes.c_int, [_i32, _i32, _i32, ctypes.POINTER(_vp),
+                                                 ctypes.POINTER(_vp), _i32, _i32, _vp, _vp, _vp]),
     "dion3_trace_collect": (ctypes.c_int, [ctypes.POINTER(_TraceEntry), _i32, ctypes.POINTER(_i32)]),
 }
 
@@ -249,6 +251,25 @@ def select_rows(momentum: Sequence, grads: Optional[Sequence], k: int, idx_out, 
     _check(load_library().dion3_select_rows(
         rows, cols, n, M, G, gd, k, _ptr(idx_out), _ptr(fro2_out), _ptr(ws), nbytes,
         _stream(stream)))
+
+
+#: Largest batch * rows dion3_select_rows_noalloc accepts (its static scratch).
+NOALLOC_MAX_ROWS = 1 << 20
+
+
+def select_rows_noalloc(momentum: Sequence, grads: Optional[Sequence], k: int, idx_out, fro2_out,
+                        stream=None):
+    """Step (a) without a workspace, for callers that may not allocate device
+    memory while stepping (see dion3_select_rows_noalloc).  Uses a static
+    8 MiB scratch inside the library: batch * rows <= NOALLOC_MAX_ROWS, and
+    calls that overlap on the GPU race on it."""
+    n = len(momentum)
+    rows, cols = momentum[0].shape
+    M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momentum])
+    G = (ctypes.c_void_p * n)(*[_ptr(t) for t in grads]) if grads is not None else None
+    gd = _dtype_code(grads[0]) if grads is not None else F32
+    _check(load_library().dion3_select_rows_noalloc(
+        rows, cols, n, M, G, gd, k, _ptr(idx_out), _ptr(fro2_out), _stream(stream)))
 
 
 def gram_ns_batched(X, O, hp: HParams, ws, stream=None, ws_bytes: Optional[int] = None):

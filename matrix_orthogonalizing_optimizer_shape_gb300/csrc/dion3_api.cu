@@ -421,6 +421,9 @@ dion3_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 }  // namespace
+
+void set_last_error_message(const char* msg) { t_last_error = msg != nullptr ? msg : ""; }
+
 }  // namespace dion3
 
 using namespace dion3;

@@ -107,4 +107,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
 // Status word address on the current device (set up by the API unit).
 unsigned* device_status_ptr();
 
+// Sets the message dion3_last_error() returns on this host thread.
+void set_last_error_message(const char* msg);
+
 }  // namespace dion3
