@@ -19,10 +19,16 @@
 //   Q <- Z Q, T = R Z, R <- Z T  (B symmetric, so B^T = B; kSymLower)
 //   Y_new^T = Y^T Q, O = (Y^T Q)^T  (A = Y^T, B = Q, kRect)
 //
-// Kernel: persistent (one CTA per SM, tiles handed out round-robin over the
-// whole batch), 128 x 256 output tiles, 6 warps with fixed roles:
+// Kernel: persistent clusters of two CTAs (one CTA per SM).  A cluster owns a
+// 256 x 256 super-tile at a time, handed out round-robin over the whole batch;
+// CTA rank r computes its rows 128 r .. 128 r + 127 as one 128 x 256 tile.  The
+// two tiles share their B panel: each CTA loads its own A tile and one half of
+// B, and multicasts that half into both CTAs' shared memory, so a 64-wide K
+// slab costs 32 KB of L2 traffic per CTA instead of 48 KB.  6 warps per CTA:
 //   warp 0 lane 0  TMA producer: 128-byte-swizzled 64-wide K slabs of A (128
-//                  rows) and B (256 rows) into a 4-deep shared-memory ring;
+//                  rows, own) and half of B (128 rows, multicast to the pair)
+//                  into a 4-deep shared-memory ring; a ring slot is refilled
+//                  only after the MMAs of BOTH CTAs have read it;
 //   warp 1         allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //                  (cta_group::1, kind::f16, M = 128, N = 256, K = 16) into one
 //                  of two 256-column fp32 accumulators, so the epilogue of a
@@ -55,7 +61,8 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 struct GemmParams {
   int M, N, K, mode;
   int tiles_r, tiles_c;      // row (128) and column (256) tile counts of one matrix
-  int tiles_per_mat, total_tiles;
+  int pairs_r;               // super-tile rows (256) of one matrix
+  int units_per_mat, total_units;  // super-tiles per matrix / in the launch
   float alpha, beta, gamma;
   const __half* C; long long c_bs; int ldc;
   __half* out; long long out_bs; int ld_out;
@@ -122,6 +129,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Multicast variant: the box lands at the same shared-memory offset in every
+// CTA of `mask`, and each destination CTA's mbarrier at offset `bar` receives
+// the completed bytes.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                      int c1, int c2, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the cluster (each warp reconverges first: the
+// barrier instructions are .aligned).
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
                : "memory");
@@ -151,6 +183,15 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` of every CTA in `mask` once this
+// thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -194,22 +235,23 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Tile t of one matrix -> (row tile bi, column tile bc).  kSymLower keeps
-// the tiles that meet the lower triangle: 128 bi + 127 >= 256 bc, i.e.
-// bi >= 2 bc, enumerated column by column.
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& bi, int& bc) {
+// Super-tile u of one matrix -> (super-row P, column tile bc); the CTA of
+// rank r computes row tile 2 P + r.  kSymLower keeps the super-tiles that meet
+// the lower triangle: 256 P + 255 >= 256 bc, i.e. P >= bc, enumerated column by
+// column.
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& P, int& bc) {
   if (p.mode == kSymLower) {
     bc = 0;
     for (;;) {
-      const int cnt = p.tiles_r - 2 * bc;
-      if (t < cnt) break;
-      t -= cnt;
+      const int cnt = p.pairs_r - bc;
+      if (u < cnt) break;
+      u -= cnt;
       ++bc;
     }
-    bi = 2 * bc + t;
+    P = bc + u;
   } else {
-    bi = t / p.tiles_c;
-    bc = t % p.tiles_c;
+    P = u / p.tiles_c;
+    bc = u % p.tiles_c;
   }
 }
 
@@ -295,7 +337,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int bidx, in
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -313,11 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.K + BK - 1) / BK;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 2);  // both CTAs' MMAs release a slot
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
@@ -328,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers are initialised before any multicast copy or remote
+  // arrive can reach them.
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -337,10 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- TMA producer ----------------
       uint32_t kc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const int bidx = t / p.tiles_per_mat;
-        int bi, bc;
-        tile_coords(p, t % p.tiles_per_mat, bi, bc);
+      for (int u = cluster; u < p.total_units && ok; u += nclusters) {
+        const int bidx = u / p.units_per_mat;
+        int P, bc;
+        unit_coords(p, u % p.units_per_mat, P, bc);
+        const int bi = 2 * P + static_cast<int>(rank);
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, p.status)) {
@@ -349,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(bar_full + 8 * s, Smem::kStageBytes);
           tma_load_3d(sA + s * Smem::kABytes, &tmA, bar_full + 8 * s, kb * BK, bi * BM, bidx);
-          tma_load_3d(sB + s * Smem::kBBytes, &tmB, bar_full + 8 * s, kb * BK, bc * BN, bidx);
+          tma_load_3d_multicast(sB + s * Smem::kBBytes + rank * (Smem::kBBytes / 2), &tmB, bar_full + 8 * s,
+                                kb * BK, bc * BN + static_cast<int>(rank) * (BN / 2), bidx, kPair);
         }
       }
       // Wait (bounded) until every copy issued into the ring has landed, so no
@@ -365,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_f16_f32();
       uint32_t kc = 0, tc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++tc) {
+      for (int u = cluster; u < p.total_units && ok; u += nclusters, ++tc) {
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
         tc_fence_after();
@@ -382,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_f16_ss(d, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar_empty + 8 * s);
+          mma_commit_multicast(bar_empty + 8 * s, kPair);
         }
         mma_commit(bar_tfull + 8 * acc);
       }
@@ -394,10 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
     uint32_t tc = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tc) {
-      const int bidx = t / p.tiles_per_mat;
-      int bi, bc;
-      tile_coords(p, t % p.tiles_per_mat, bi, bc);
+    for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
+      const int bidx = u / p.units_per_mat;
+      int P, bc;
+      unit_coords(p, u % p.units_per_mat, P, bc);
+      const int bi = 2 * P + static_cast<int>(rank);
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
       if (!ok) break;
@@ -418,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  // Neither CTA leaves while its peer may still multicast into its shared
+  // memory or arrive on its barriers.
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -459,14 +511,22 @@ bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, in
   return r == CUDA_SUCCESS;
 }
 
-int sm_count() {
+// Clusters of this kernel that fit on the device at once (persistent grid).
+int max_active_clusters(int dev) {
   static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
   if (cached[dev & 63] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Smem::kDyn;
     int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev & 63] = n > 0 ? n : 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      n = sms > 1 ? sms / 2 : 1;
+    }
+    cached[dev & 63] = n;
   }
   return cached[dev & 63];
 }
@@ -504,7 +564,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
 
   CUtensorMap ta, tb;
   if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2)) return cudaErrorInvalidValue;
 
   GemmParams p{};
   p.M = g.M;
@@ -513,16 +573,16 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.mode = g.mode;
   p.tiles_r = (g.M + BM - 1) / BM;
   p.tiles_c = (g.N + BN - 1) / BN;
+  p.pairs_r = (p.tiles_r + 1) / 2;
   if (g.mode == kSymLower) {
-    long long cnt = 0;
-    for (int bc = 0; 2 * bc < p.tiles_r; ++bc) cnt += p.tiles_r - 2 * bc;
-    p.tiles_per_mat = static_cast<int>(cnt);
+    // BN == 2 BM: super-tile rows and column tiles have the same 256 extent.
+    p.units_per_mat = p.pairs_r * (p.pairs_r + 1) / 2;
   } else {
-    p.tiles_per_mat = p.tiles_r * p.tiles_c;
+    p.units_per_mat = p.pairs_r * p.tiles_c;
   }
-  const long long total = static_cast<long long>(p.tiles_per_mat) * g.batch;
+  const long long total = static_cast<long long>(p.units_per_mat) * g.batch;
   if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  p.total_tiles = static_cast<int>(total);
+  p.total_units = static_cast<int>(total);
   p.alpha = g.alpha;
   p.beta = g.beta;
   p.gamma = g.gamma;
@@ -537,7 +597,8 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.ld_outT = g.ld_outT;
   p.status = dev_status;
 
-  const int grid = static_cast<int>(std::min<long long>(total, sm_count()));
+  const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
+  const int grid = 2 * clusters;
   kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, p);
   return cudaGetLastError();
 }
