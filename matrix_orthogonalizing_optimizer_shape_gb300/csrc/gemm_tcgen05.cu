@@ -19,26 +19,27 @@
 //   Q <- Z Q, T = R Z, R <- Z T  (B symmetric, so B^T = B; kSymLower)
 //   Y_new^T = Y^T Q, O = (Y^T Q)^T  (A = Y^T, B = Q, kRect)
 //
-// Kernel: persistent clusters of two CTAs (one CTA per SM).  A cluster owns a
-// 256 x 256 super-tile at a time, handed out round-robin over the whole batch;
-// CTA rank r computes its rows 128 r .. 128 r + 127 as one 128 x 256 tile.  The
-// two tiles share their B panel: each CTA loads its own A tile and one half of
-// B, and multicasts that half into both CTAs' shared memory, so a 64-wide K
-// slab costs 32 KB of L2 traffic per CTA instead of 48 KB.  6 warps per CTA:
-//   warp 0 lane 0  TMA producer: 128-byte-swizzled 64-wide K slabs of A (128
-//                  rows, own) and half of B (128 rows, multicast to the pair)
-//                  into a 4-deep shared-memory ring; a ring slot is refilled
-//                  only after the MMAs of BOTH CTAs have read it;
-//   warp 1         allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//                  (cta_group::1, kind::f16, M = 128, N = 256, K = 16) into one
-//                  of two 256-column fp32 accumulators, so the epilogue of a
-//                  tile overlaps the main loop of the next;
-//   warps 2..5     epilogue: tcgen05.ld of the 32 TMEM lanes each warp may
-//                  access (warp % 4), alpha/beta/gamma, fp16 stores.
+// Kernel: persistent clusters of two CTAs on two SMs (a CTA pair), one CTA
+// per SM.  A cluster owns a 256 x 256 super-tile at a time, handed out
+// round-robin over the whole batch, and computes it with the paired-SM MMA
+// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16): CTA rank r holds rows
+// 128 r .. 128 r + 127 of A and rows 128 r .. 128 r + 127 of the B panel in its
+// own shared memory, and receives rows 128 r .. of the result in its own TMEM.
+// A ring slot therefore holds 32 KB per CTA (its A tile and its half of B), so
+// the 192 KB ring is 6 slots deep.  6 warps per CTA:
+//   warp 0 lane 0  TMA producer (both CTAs): fills the CTA's own slot and
+//                  signals the even CTA's "full" barrier (cta_group::2 copy);
+//   warp 1         allocates 512 TMEM columns for the pair (both CTAs); in the
+//                  even CTA lane 0 issues the paired MMAs into one of two
+//                  256-column fp32 accumulators and releases ring slots and
+//                  accumulators in both CTAs with multicast commits;
+//   warps 2..5     epilogue (both CTAs): tcgen05.ld of the 32 TMEM lanes each
+//                  warp may access (warp % 4), alpha/beta/gamma, fp16 stores;
+//                  then they tell the even CTA that the accumulator is free.
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that runs out sets a bit in the device status word and the CTA winds down:
-// the producer waits (bounded) for its copies in flight, the MMA issuer for
-// its MMAs, and the TMEM is freed on every path.
+// the issuing CTA waits (bounded) for its MMAs, both CTAs meet at a cluster
+// barrier before freeing TMEM, and TMEM is freed on every path.
 #include "internal.h"
 
 #include <cuda.h>
@@ -53,7 +54,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;  // fp16 elements per 128-byte swizzle row
 constexpr int BN = 256;
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -99,7 +100,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -129,16 +130,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset in every
-// CTA of `mask`, and each destination CTA's mbarrier at offset `bar` receives
-// the completed bytes.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                                      int c1, int c2, uint16_t mask) {
+// Paired-SM variant: the box lands in this CTA's shared memory and the
+// completed bytes are reported to an mbarrier that may live in the peer CTA
+// (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -154,14 +168,15 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+// Paired allocation: one warp of each CTA of the pair executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -171,24 +186,22 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// Paired-SM MMA: A and B descriptors name the same shared-memory offsets in
+// both CTAs of the pair; D is the same TMEM address in both.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // Arrive on the mbarrier at offset `bar` of every CTA in `mask` once this
-// thread's earlier MMAs have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+// thread's earlier paired MMAs have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                    bar),
                "h"(mask)
                : "memory");
@@ -226,9 +239,9 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
+// M >> 4 in bits 24-28; M = 256 for the paired MMA (128 rows per CTA).
 __device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
-  return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -257,7 +270,7 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& P, 
 
 struct Smem {
   static constexpr int kABytes = BM * BK * 2;   // 16 KB
-  static constexpr int kBBytes = BN * BK * 2;   // 32 KB
+  static constexpr int kBBytes = (BN / 2) * BK * 2;   // this CTA's half of B: 16 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain
@@ -356,22 +369,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.K + BK - 1) / BK;
   const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;  // issues the pair's MMAs
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 2);  // both CTAs' MMAs release a slot
+      mbar_init(bar_full + 8 * s, 1);   // used in the even CTA: its producer + both CTAs' bytes
+      mbar_init(bar_empty + 8 * s, 1);  // the pair's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, 128);
+      mbar_init(bar_tempty + 8 * a, 256);  // used in the even CTA: both CTAs' epilogue threads
     }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   // Both CTAs' barriers are initialised before any multicast copy or remote
   // arrive can reach them.
@@ -395,21 +409,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar_full + 8 * s, Smem::kStageBytes);
-          tma_load_3d(sA + s * Smem::kABytes, &tmA, bar_full + 8 * s, kb * BK, bi * BM, bidx);
-          tma_load_3d_multicast(sB + s * Smem::kBBytes + rank * (Smem::kBBytes / 2), &tmB, bar_full + 8 * s,
-                                kb * BK, bc * BN + static_cast<int>(rank) * (BN / 2), bidx, kPair);
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Smem::kStageBytes);
+          const uint32_t full_even = map_to_rank(bar_full + 8 * s, 0);
+          tma_load_3d_pair(sA + s * Smem::kABytes, &tmA, full_even, kb * BK, bi * BM, bidx);
+          tma_load_3d_pair(sB + s * Smem::kBBytes, &tmB, full_even, kb * BK,
+                           bc * BN + static_cast<int>(rank) * (BN / 2), bidx);
         }
       }
       // Wait (bounded) until every copy issued into the ring has landed, so no
-      // copy is in flight when the CTA exits.
-      for (uint32_t i = 0; i < kStages && i < kc; ++i) {
+      // copy is in flight when the pair exits (the even CTA's barriers count
+      // the bytes of both CTAs).
+      for (uint32_t i = 0; leader && i < kStages && i < kc; ++i) {
         const uint32_t last = kc - 1 - i;  // most recent fill of stage last % kStages
         mbar_wait(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc = idesc_f16_f32();
       uint32_t kc = 0, tc = 0;
@@ -430,13 +446,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t db = sdesc_kmajor_sw128(sB + s * Smem::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_ss(d, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_multicast(bar_empty + 8 * s, kPair);
+            mma_f16_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(bar_empty + 8 * s, kPair);
         }
-        mma_commit(bar_tfull + 8 * acc);
+        mma_commit_pair(bar_tfull + 8 * acc, kPair);
       }
       // All MMAs issued by this thread complete before TMEM is freed.
-      mma_commit(bar_drain);
+      mma_commit_pair(bar_drain, 0x1);
       mbar_wait(bar_drain, 0u, p.status);
     }
   } else {
@@ -464,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_chunk(p, bidx, r, c0, row0, v);
       }
       tc_fence_before();
-      mbar_arrive(bar_tempty + 8 * acc);
+      mbar_arrive_cluster(map_to_rank(bar_tempty + 8 * acc, 0));
     }
   }
   tc_fence_before();
@@ -473,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
