@@ -171,6 +171,37 @@ dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const vo
                                    void* O, const dion3_hparams* hp, void* ws,
                                    size_t ws_bytes, dion3_stream_t stream);
 
+/*
+ * Newton-Schulz variants on the same tensor-core kernels, for the comparison
+ * the first-level paragraph of the summary page makes (Gram NS saves 55 % of
+ * the FLOPs of standard NS with symmetric GEMMs and 68 % of the common
+ * implementation without them):
+ *   DION3_NS_GRAM            Gram NS, symmetric products on lower tiles (the
+ *                            same computation as dion3_gram_ns_batched);
+ *   DION3_NS_GRAM_DENSE      Gram NS with every tile of every product;
+ *   DION3_NS_STANDARD        standard NS on X (A = X X^T, B = bA + cA^2,
+ *                            X <- aX + BX) with symmetric A and A^2;
+ *   DION3_NS_STANDARD_DENSE  standard NS with every tile computed.
+ * dion3_ns_batched has the arguments and results of dion3_gram_ns_batched
+ * plus the variant; restart_iter applies to the Gram variants only.
+ * dion3_ns_useful_flops counts a computed triangle as half, full tiles in
+ * full (so the dense variants count every product in full); negative on
+ * invalid arguments.
+ */
+typedef enum {
+  DION3_NS_GRAM = 0,
+  DION3_NS_GRAM_DENSE = 1,
+  DION3_NS_STANDARD = 2,
+  DION3_NS_STANDARD_DENSE = 3
+} dion3_ns_variant;
+
+double dion3_ns_useful_flops(int32_t variant, int32_t k, int32_t m, const dion3_hparams* hp);
+dion3_status dion3_ns_workspace_size(int32_t variant, int32_t k, int32_t m, int32_t batch,
+                                     const dion3_hparams* hp, size_t* bytes);
+dion3_status dion3_ns_batched(int32_t variant, int32_t k, int32_t m, int32_t batch, const void* X,
+                              void* O, const dion3_hparams* hp, void* ws, size_t ws_bytes,
+                              dion3_stream_t stream);
+
 typedef enum { DION3_GEMM_RECT = 0, DION3_GEMM_SYM_LOWER = 1 } dion3_gemm_mode;
 
 /*

@@ -38,7 +38,8 @@ EXPORTED = (
     "dion3_useful_flops", "dion3_select_workspace_size", "dion3_select_rows",
     "dion3_gram_ns_workspace_size", "dion3_gram_ns_batched", "dion3_workspace_size",
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
-    "dion3_trace_collect", "dion3_select_rows_noalloc",
+    "dion3_trace_collect", "dion3_select_rows_noalloc", "dion3_ns_useful_flops",
+    "dion3_ns_workspace_size", "dion3_ns_batched",
 )
 
 
@@ -96,6 +97,11 @@ _SIGS = {
                                       _vp, _i32, ctypes.c_int64,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, _vp]),
     "dion3_trace_enable": (ctypes.c_int, [_i32]),
+    "dion3_ns_useful_flops": (ctypes.c_double, [_i32, _i32, _i32, ctypes.POINTER(_HParams)]),
+    "dion3_ns_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, ctypes.POINTER(_HParams),
+                                               ctypes.POINTER(_sz)]),
+    "dion3_ns_batched": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, ctypes.POINTER(_HParams),
+                                        _vp, _sz, _vp]),
     "dion3_select_rows_noalloc": (ctypes.c_int, [_i32, _i32, _i32, ctypes.POINTER(_vp),
                                                  ctypes.POINTER(_vp), _i32, _i32, _vp, _vp, _vp]),
     "dion3_trace_collect": (ctypes.c_int, [ctypes.POINTER(_TraceEntry), _i32, ctypes.POINTER(_i32)]),
@@ -295,6 +301,35 @@ def step(groups: Sequence[Group], hp: HParams, ws, sel_idx_out: Optional[Sequenc
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     _check(load_library().dion3_step(cg, len(groups), ctypes.byref(hs), _ptr(ws), nbytes, sel,
                                      _stream(stream)))
+
+
+NS_GRAM, NS_GRAM_DENSE, NS_STANDARD, NS_STANDARD_DENSE = 0, 1, 2, 3
+
+
+def ns_useful_flops(variant: int, k: int, m: int, hp: HParams) -> float:
+    hs = hp.c_struct()
+    return float(load_library().dion3_ns_useful_flops(variant, k, m, ctypes.byref(hs)))
+
+
+def ns_workspace_size(variant: int, k: int, m: int, batch: int, hp: HParams) -> int:
+    out = ctypes.c_size_t(0)
+    hs = hp.c_struct()
+    _check(load_library().dion3_ns_workspace_size(variant, k, m, batch, ctypes.byref(hs),
+                                                  ctypes.byref(out)))
+    return out.value
+
+
+def ns_batched(variant: int, X, O, hp: HParams, ws, stream=None, ws_bytes: Optional[int] = None):
+    """Newton-Schulz variant `variant` of fp16 X [batch, k, m] into O (see
+    dion3_ns_batched)."""
+    if X.dim() == 2:
+        batch, (k, m) = 1, X.shape
+    else:
+        batch, k, m = X.shape
+    hs = hp.c_struct()
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(load_library().dion3_ns_batched(variant, k, m, batch, _ptr(X), _ptr(O), ctypes.byref(hs),
+                                           _ptr(ws), nbytes, _stream(stream)))
 
 
 GEMM_RECT, GEMM_SYM_LOWER = 0, 1

@@ -282,7 +282,7 @@ struct NsOut {
 };
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool dense = false) {
   auto sym = [&](const __half* A, const __half* B, __half* D, int K, const __half* C, float alpha, float beta,
                  float gamma, const __half* Abase_is_Y) -> GemmDesc {
     GemmDesc g{};
@@ -290,7 +290,9 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     g.A = A; g.a_bstride = from_y ? p.y_bs : p.s_bs; g.lda = from_y ? p.Lp : p.sp;
     g.B = B; g.b_bstride = from_y ? p.y_bs : p.s_bs; g.ldb = from_y ? p.Lp : p.sp;
     g.M = p.s; g.N = p.s; g.K = K; g.batch = p.batch;
-    g.mode = kSymLower;
+    // dense: every tile of the product (the comparison path without the
+    // symmetric savings); otherwise lower-triangle tiles, mirrored.
+    g.mode = dense ? kRect : kSymLower;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
     g.C = C; g.c_bstride = p.s_bs; g.ldc = p.sp;
     g.out = D; g.out_bstride = p.s_bs; g.ld_out = p.sp;
@@ -361,6 +363,120 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     g.out = out.O; g.out_bstride = out.o_bs; g.ld_out = out.ld_o;
   }
   return launch(g);
+}
+
+// ---------------------------------------------------------------------------
+// Standard Newton-Schulz on the same kernels (the comparison path of the
+// first-level paragraph of the summary page: the common implementation that
+// iterates on X itself).  Per iteration on Y (s x L, s <= L):
+//   A = Y Y^T;  B = c A.A + b A;  Y <- a Y + B Y
+// with Y and Y^T ping-ponged so every operand is K-major; the last iteration
+// writes O in X's orientation.
+// ---------------------------------------------------------------------------
+struct StdPlan {
+  int k, m, batch, s, L, sp, Lp;
+  bool wide;
+  __half* Y[2];
+  __half* Yt[2];
+  __half* S[2];
+  long long y_bs, yt_bs, s_bs;
+};
+
+void plan_std(Carver& c, int k, int m, int batch, StdPlan& p) {
+  p.k = k;
+  p.m = m;
+  p.batch = batch;
+  p.wide = k <= m;
+  p.s = p.wide ? k : m;
+  p.L = p.wide ? m : k;
+  p.sp = static_cast<int>(round_up(p.s, 8));
+  p.Lp = static_cast<int>(round_up(p.L, 8));
+  p.y_bs = static_cast<long long>(p.s) * p.Lp;
+  p.yt_bs = static_cast<long long>(p.L) * p.sp;
+  p.s_bs = static_cast<long long>(p.s) * p.sp;
+  for (int i = 0; i < 2; ++i) p.Y[i] = c.take<__half>(p.y_bs * batch);
+  for (int i = 0; i < 2; ++i) p.Yt[i] = c.take<__half>(p.yt_bs * batch);
+  for (int i = 0; i < 2; ++i) p.S[i] = c.take<__half>(p.s_bs * batch);
+}
+
+void gather_targets_std(const StdPlan& p, GatherArgs& g) {
+  if (p.wide) {
+    g.out_rows = p.Y[0];   g.rows_bstride = p.y_bs;  g.ld_rows = p.Lp;
+    g.out_cols = p.Yt[0];  g.cols_bstride = p.yt_bs; g.ld_cols = p.sp;
+  } else {
+    g.out_rows = p.Yt[0];  g.rows_bstride = p.yt_bs; g.ld_rows = p.sp;
+    g.out_cols = p.Y[0];   g.cols_bstride = p.y_bs;  g.ld_cols = p.Lp;
+  }
+}
+
+dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
+                             cudaStream_t stream, bool dense) {
+  auto launch = [&](const GemmDesc& g) -> dion3_status {
+    const char* why = nullptr;
+    if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
+    const cudaError_t e = traced_gemm(g, st, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return DION3_OK;
+  };
+  const int mode_sym = dense ? kRect : kSymLower;
+  dion3_status rc;
+  for (int t = 0; t < hp.ns_steps; ++t) {
+    const int cur = t & 1, nxt = cur ^ 1;
+    const bool last = t + 1 == hp.ns_steps;
+    // A = Y Y^T
+    GemmDesc g1{};
+    g1.A = p.Y[cur]; g1.a_bstride = p.y_bs; g1.lda = p.Lp;
+    g1.B = p.Y[cur]; g1.b_bstride = p.y_bs; g1.ldb = p.Lp;
+    g1.M = p.s; g1.N = p.s; g1.K = p.L; g1.batch = p.batch;
+    g1.mode = mode_sym; g1.alpha = 1.f;
+    g1.out = p.S[0]; g1.out_bstride = p.s_bs; g1.ld_out = p.sp;
+    if ((rc = launch(g1)) != DION3_OK) return rc;
+    // B = c A.A + b A
+    GemmDesc g2{};
+    g2.A = p.S[0]; g2.a_bstride = p.s_bs; g2.lda = p.sp;
+    g2.B = p.S[0]; g2.b_bstride = p.s_bs; g2.ldb = p.sp;
+    g2.M = p.s; g2.N = p.s; g2.K = p.s; g2.batch = p.batch;
+    g2.mode = mode_sym; g2.alpha = hp.c; g2.beta = hp.b;
+    g2.C = p.S[0]; g2.c_bstride = p.s_bs; g2.ldc = p.sp;
+    g2.out = p.S[1]; g2.out_bstride = p.s_bs; g2.ld_out = p.sp;
+    if ((rc = launch(g2)) != DION3_OK) return rc;
+    // Y <- a Y + B Y:  D = B (Y^T)^T, C = Y
+    GemmDesc g3{};
+    g3.A = p.S[1]; g3.a_bstride = p.s_bs; g3.lda = p.sp;
+    g3.B = p.Yt[cur]; g3.b_bstride = p.yt_bs; g3.ldb = p.sp;
+    g3.M = p.s; g3.N = p.L; g3.K = p.s; g3.batch = p.batch;
+    g3.mode = kRect; g3.alpha = 1.f; g3.beta = hp.a;
+    g3.C = p.Y[cur]; g3.c_bstride = p.y_bs; g3.ldc = p.Lp;
+    if (!last) {
+      g3.out = p.Y[nxt]; g3.out_bstride = p.y_bs; g3.ld_out = p.Lp;
+      g3.outT = p.Yt[nxt]; g3.outT_bstride = p.yt_bs; g3.ld_outT = p.sp;
+    } else if (p.wide) {
+      g3.out = out.O; g3.out_bstride = out.o_bs; g3.ld_out = out.ld_o;
+    } else {
+      g3.outT = out.O; g3.outT_bstride = out.o_bs; g3.ld_outT = out.ld_o;
+    }
+    if ((rc = launch(g3)) != DION3_OK) return rc;
+  }
+  return DION3_OK;
+}
+
+// Useful FLOPs of each variant (a computed triangle counts half; the dense
+// variants compute every tile, so their products count in full).
+double variant_flops(int variant, int k, int m, const dion3_hparams& hp) {
+  const double s = std::min(k, m), L = std::max(k, m), T = hp.ns_steps;
+  switch (variant) {
+    case DION3_NS_GRAM: return schedule_flops(k, m, hp);
+    case DION3_NS_GRAM_DENSE: {
+      // every product of the Gram schedule in full: SYRK 2 s^2 L, square 2 s^3
+      const double sym = schedule_flops(k, m, hp);
+      const int restarts = (hp.restart_iter > 1) ? 1 : 0;
+      const double syrk = s * s * L * (1 + restarts), rect = 2.0 * s * s * L * (1 + restarts);
+      return 2.0 * (sym - syrk - rect) + 2.0 * syrk + rect;
+    }
+    case DION3_NS_STANDARD: return T * (3.0 * s * s * L + s * s * s);
+    case DION3_NS_STANDARD_DENSE: return T * (4.0 * s * s * L + 2.0 * s * s * s);
+    default: return -1.0;
+  }
 }
 
 // Step workspace layout for one group.
@@ -555,6 +671,72 @@ dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const vo
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
   NsOut out{static_cast<__half*>(O), static_cast<long long>(k) * m, m};
   if ((rc = run_gram_ns(p, *hp, out, st, s)) != DION3_OK) return rc;
+  return ok();
+}
+
+double dion3_ns_useful_flops(int32_t variant, int32_t k, int32_t m, const dion3_hparams* hp) {
+  if (k < 1 || m < 1 || check_hparams(hp, false) != DION3_OK) return -1.0;
+  return variant_flops(variant, k, m, *hp);
+}
+
+dion3_status dion3_ns_workspace_size(int32_t variant, int32_t k, int32_t m, int32_t batch,
+                                     const dion3_hparams* hp, size_t* bytes) {
+  if (variant == DION3_NS_GRAM || variant == DION3_NS_GRAM_DENSE)
+    return dion3_gram_ns_workspace_size(k, m, batch, hp, bytes);
+  if (variant != DION3_NS_STANDARD && variant != DION3_NS_STANDARD_DENSE)
+    return fail(DION3_ERR_INVALID_ARG, "unknown Newton-Schulz variant %d", variant);
+  if (bytes == nullptr) return fail(DION3_ERR_INVALID_ARG, "bytes is NULL");
+  if (k < 1 || m < 1 || batch < 1 || batch > 65535)
+    return fail(DION3_ERR_INVALID_ARG, "need k, m >= 1 and 1 <= batch <= 65535");
+  dion3_status rc = check_hparams(hp, false);
+  if (rc != DION3_OK) return rc;
+  Carver c{nullptr};
+  StdPlan p;
+  plan_std(c, k, m, batch, p);
+  c.take<float>(static_cast<long long>(batch) * 64);
+  *bytes = round_up(static_cast<long long>(c.off), 256);
+  return ok();
+}
+
+dion3_status dion3_ns_batched(int32_t variant, int32_t k, int32_t m, int32_t batch, const void* X, void* O,
+                              const dion3_hparams* hp, void* ws, size_t ws_bytes, dion3_stream_t stream) {
+  size_t need = 0;
+  dion3_status rc = dion3_ns_workspace_size(variant, k, m, batch, hp, &need);
+  if (rc != DION3_OK) return rc;
+  if (X == nullptr || O == nullptr) return fail(DION3_ERR_INVALID_ARG, "X and O must not be NULL");
+  if (!aligned16(X) || !aligned16(O)) return fail(DION3_ERR_INVALID_ARG, "X and O must be 16-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Carver c{static_cast<char*>(ws)};
+  GatherArgs g{};
+  NsPlan gp;
+  StdPlan sp;
+  const bool gram = variant == DION3_NS_GRAM || variant == DION3_NS_GRAM_DENSE;
+  if (gram) {
+    plan_ns(c, k, m, batch, gp);
+    gather_targets(gp, g);
+  } else {
+    plan_std(c, k, m, batch, sp);
+    gather_targets_std(sp, g);
+  }
+  constexpr int kParts = 64;
+  float* parts = c.take<float>(static_cast<long long>(batch) * kParts);
+  const long long n = static_cast<long long>(k) * m;
+  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sumsq launch");
+  g.k = k; g.m = m; g.batch = batch; g.src_f32 = false;
+  g.X = static_cast<const __half*>(X);
+  g.fro2 = parts; g.fro2_parts = kParts; g.eps = hp->eps; g.decay = false;
+  g.n = k; g.status = st;
+  e = traced_gather(g, m % 4 == 0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  NsOut out{static_cast<__half*>(O), static_cast<long long>(k) * m, m};
+  rc = gram ? run_gram_ns(gp, *hp, out, st, s, variant == DION3_NS_GRAM_DENSE)
+            : run_standard_ns(sp, *hp, out, st, s, variant == DION3_NS_STANDARD_DENSE);
+  if (rc != DION3_OK) return rc;
   return ok();
 }
 

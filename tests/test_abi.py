@@ -168,3 +168,18 @@ def test_workspace_grows_with_batch(lib):
     sizes = [d3.gram_ns_workspace_size(256, 1024, b, hp) for b in (1, 2, 8)]
     assert sizes[0] < sizes[1] < sizes[2]
     assert d3.select_workspace_size(1024, 4096, 1, 256) >= 2 * 1024 * 4
+
+
+@pytest.mark.parametrize("k,m", [(256, 1024), (1024, 256), (2752, 4096), (96, 96)])
+def test_variant_flops_match_oracle(lib, k, m):
+    from oracle import standard_ns_dense_flops, standard_ns_useful_flops
+    hp = d3.HParams(ns_steps=5, restart_iter=3)
+    s, L = min(k, m), max(k, m)
+    assert d3.ns_useful_flops(d3.NS_STANDARD, k, m, hp) == standard_ns_useful_flops(s, L, 5)
+    assert d3.ns_useful_flops(d3.NS_STANDARD_DENSE, k, m, hp) == standard_ns_dense_flops(s, L, 5)
+    assert d3.ns_useful_flops(d3.NS_GRAM, k, m, hp) == d3.useful_flops(k, m, hp)
+    log = []
+    gram_newton_schulz(np.ones((2, 3)) / 6.0, MUON_QUINTIC, 5, restart_iter=3, op_log=log)
+    dense = sum(2.0 * s * s * L if op[0] in ("syrk", "rect") else 2.0 * s ** 3 for op in log)
+    assert d3.ns_useful_flops(d3.NS_GRAM_DENSE, k, m, hp) == dense
+    assert d3.ns_useful_flops(7, k, m, hp) < 0

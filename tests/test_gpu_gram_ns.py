@@ -72,3 +72,21 @@ def test_gram_ns_output_singular_values_band(cuda_lib):
     O = _run(X, d3.HParams())
     sv = np.linalg.svd(O[0].astype(np.float64), compute_uv=False)
     assert sv.min() > 0.6 and sv.max() < 1.25
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("k,m", [(200, 520), (520, 200), (256, 256)])
+def test_ns_variants_match_oracle(cuda_lib, variant, k, m):
+    # Gram NS (symmetric / dense) and standard NS (symmetric / dense) on the
+    # same kernels all compute the oracle's standard quintic NS.
+    X = _inputs(2, k, m, seed=variant * 100 + k)
+    hp = d3.HParams()
+    Xd = torch.from_numpy(X).to("cuda").half().contiguous()
+    O = torch.full_like(Xd, float("nan"))
+    ws = d3.alloc_workspace(d3.ns_workspace_size(variant, k, m, 2, hp))
+    d3.ns_batched(variant, Xd, O, hp, ws)
+    d3.device_status()
+    O = O.float().cpu().numpy()
+    for b in range(2):
+        want = newton_schulz(normalize(X[b], hp.eps), MUON_QUINTIC, 5)
+        assert rel_fro(O[b], want) <= O_REL_FRO, (variant, k, m, b)
