@@ -336,6 +336,119 @@ def run_ours(args, rank, world, device_index):
 
 
 # ---------------------------------------------------------------------------
+# Gram-NS sweep: fp16 Gaussian X, s x L with L = s * aspect, batch of same-shape
+# matrices; our four Newton-Schulz variants and cuBLAS (torch fp16 bmm)
+# running the Gram schedule and standard NS as reference points.
+# ---------------------------------------------------------------------------
+
+def _cublas_gram_ns(X, hp):
+    """Gram NS with torch fp16 batched matmuls (cuBLAS), same schedule."""
+    import torch
+    a, b, c = hp.coeffs
+    Y = X / (X.float().pow(2).sum(dim=(1, 2), keepdim=True).sqrt().half() + hp.eps)
+    s = Y.shape[1]
+    eye = torch.eye(s, device=X.device, dtype=X.dtype).expand(Y.shape[0], s, s)
+    R = torch.bmm(Y, Y.transpose(1, 2))
+    Q = None
+    for t in range(1, hp.ns_steps + 1):
+        if t == hp.restart_iter and t > 1:
+            Y = torch.bmm(Q, Y)
+            R = torch.bmm(Y, Y.transpose(1, 2))
+            Q = None
+        Z = torch.baddbmm(torch.add(eye * a, R, alpha=b), R, R, alpha=c)
+        Q = Z if Q is None else torch.bmm(Z, Q)
+        if t < hp.ns_steps and t + 1 != hp.restart_iter:
+            R = torch.bmm(Z, torch.bmm(R, Z))
+    return torch.bmm(Q, Y)
+
+
+def _cublas_standard_ns(X, hp):
+    import torch
+    a, b, c = hp.coeffs
+    Y = X / (X.float().pow(2).sum(dim=(1, 2), keepdim=True).sqrt().half() + hp.eps)
+    for _ in range(hp.ns_steps):
+        A = torch.bmm(Y, Y.transpose(1, 2))
+        B = torch.baddbmm(A * b, A, A, alpha=c)
+        Y = torch.baddbmm(Y * a, B, Y)
+    return Y
+
+
+def run_sweep(args):
+    import torch
+    import matrix_orthogonalizing_optimizer_shape_gb300 as d3
+    import workloads
+    d3.load_library()
+    hp = d3.HParams()
+    if args.sweep_full:
+        pts = [(s, a, b) for s in workloads.SWEEP_S for a in workloads.SWEEP_ASPECT
+               for b in workloads.SWEEP_BATCH]
+    else:
+        # one batch per (s, aspect), chosen for about 20 TFLOP of Gram-NS work
+        pts = []
+        for s_ in workloads.SWEEP_S:
+            for a in (1, 4):
+                L = s_ * a
+                work = 6.0 * s_ * s_ * L + 14.0 * s_ ** 3
+                b = max(1, min(64, int(2e13 // work)))
+                b = max(x for x in workloads.SWEEP_BATCH if x <= b)
+                pts.append((s_, a, b))
+    names = {d3.NS_GRAM: "gram", d3.NS_GRAM_DENSE: "gram_dense", d3.NS_STANDARD: "standard",
+             d3.NS_STANDARD_DENSE: "standard_dense"}
+    rows = []
+    s_ev = torch.cuda.current_stream()
+    for (s_, a, b) in pts:
+        L = s_ * a
+        # X + O + workspace of the largest variant must fit comfortably
+        need = 2 * b * s_ * L * 2 + max(d3.ns_workspace_size(v, s_, L, b, hp) for v in names)
+        if need > 200e9:
+            rows.append({"s": s_, "L": L, "batch": b, "skipped": "over 200 GB"})
+            continue
+        g = torch.Generator(device="cuda")
+        g.manual_seed(s_ * 131 + a * 7 + b)
+        X = torch.randn((b, s_, L), generator=g, device="cuda", dtype=torch.float32).half()
+        O = torch.empty_like(X)
+        row = {"s": s_, "L": L, "batch": b}
+        for v, name in names.items():
+            ws = d3.alloc_workspace(d3.ns_workspace_size(v, s_, L, b, hp))
+            for _ in range(2):
+                d3.ns_batched(v, X, O, hp, ws)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_ev)
+            for _ in range(args.steps):
+                d3.ns_batched(v, X, O, hp, ws)
+            e1.record(s_ev)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            row[name + "_ms"] = ms
+            row[name + "_tflops"] = b * d3.ns_useful_flops(v, s_, L, hp) / (ms * 1e-3) / 1e12
+            del ws
+        d3.device_status()
+        for name, fn in (("cublas_gram", _cublas_gram_ns), ("cublas_standard", _cublas_standard_ns)):
+            for _ in range(2):
+                fn(X, hp)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_ev)
+            for _ in range(args.steps):
+                fn(X, hp)
+            e1.record(s_ev)
+            torch.cuda.synchronize()
+            row[name + "_ms"] = e0.elapsed_time(e1) / args.steps
+        row["speedup_vs_standard"] = row["standard_ms"] / row["gram_ms"]
+        row["speedup_vs_standard_dense"] = row["standard_dense_ms"] / row["gram_ms"]
+        row["speedup_vs_cublas_standard"] = row["cublas_standard_ms"] / row["gram_ms"]
+        row["speedup_vs_cublas_gram"] = row["cublas_gram_ms"] / row["gram_ms"]
+        rows.append(row)
+        del X, O
+        torch.cuda.empty_cache()
+    peaks, src = load_peaks()
+    return {"metric": "Gram-NS sweep: ms and useful TFLOP/s per variant", "unit": "TFLOP/s",
+            "data": "synthetic", "dtype": "f16", "steps": args.steps,
+            "peak_bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"), "peak_source": src,
+            "config": {"workload": "fp16 Gaussian X, s x L, T=5 restart@3 (standard NS: T=5)"},
+            "points": rows}
+
+
+# ---------------------------------------------------------------------------
 # Reference arm: the float64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
@@ -400,7 +513,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="7b", choices=["7b", "1b", "gapped", "single"])
+    ap.add_argument("--workload", default="7b", choices=["7b", "1b", "gapped", "single", "sweep"])
+    ap.add_argument("--sweep-full", action="store_true",
+                    help="with --workload sweep: every (s, aspect, batch) of the sweep grid")
     ap.add_argument("--f", type=float, default=0.25)
     ap.add_argument("--max-batch", type=int, default=0,
                     help="cap the matrices per shape group (small profiling case)")
@@ -413,6 +528,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "sweep":
+        if rank == 0 and args.impl == "ours":
+            print(json.dumps(run_sweep(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank == 0:
