@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 namespace dion3 {
@@ -68,6 +69,7 @@ struct GemmParams {
   const __half* C; long long c_bs; int ldc;
   __half* out; long long out_bs; int ld_out;
   __half* outT; long long outT_bs; int ld_outT;
+  int tma_out, tma_outT;     // the output has a TMA store map (16-byte pitch rules hold)
   unsigned* status;
 };
 
@@ -140,6 +142,29 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Bulk tensor store of a shared-memory box to global memory (bulk-group
+// completion; out-of-range parts of the box are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one of this thread's bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes become visible to the async proxy.
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 // shared::cluster address of the same shared-memory offset in CTA `rank`.
@@ -273,22 +298,28 @@ struct Smem {
   static constexpr int kBBytes = (BN / 2) * BK * 2;   // this CTA's half of B: 16 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
+  // Epilogue staging: per epilogue warp two buffers, each a 32 x 32 fp16 box
+  // and its transpose (2 KB each), laid out with the 64-byte swizzle of the
+  // store tensor maps.
+  static constexpr int kStageBoxBytes = 32 * 32 * 2;
+  static constexpr int kWarpStagingBytes = 2 * 2 * kStageBoxBytes;
+  static constexpr int kStagingBytes = 4 * kWarpStagingBytes;
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-  static constexpr int kDyn = 1024 + kRingBytes + kBarBytes + 16;
+  static constexpr int kDyn = 1024 + kRingBytes + kStagingBytes + kBarBytes + 16;
 };
 
-// Epilogue of one 32-row x 32-column chunk held by a warp: thread `lane` owns
-// row r; v[j] is column c0 + j of the fp32 accumulator.
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int bidx, int r, int c0, int row0,
-                                               const uint32_t (&v)[32]) {
-  if (r >= p.M) return;
-  const bool sym = p.mode == kSymLower;
+// Values of one 32-row x 32-column chunk held by a warp: thread `lane` owns
+// row r; v[j] is column c0 + j of the fp32 accumulator.  hp receives
+// alpha D + beta C + gamma I as packed fp16 pairs (rows r >= M give zeros and
+// read nothing).
+__device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
+                                             uint32_t (&hp)[16]) {
   const bool full = (c0 + 32 <= p.N);
   float f[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
-  if (p.C != nullptr) {
+  if (p.C != nullptr && r < p.M) {
     const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
     if (full && (p.ldc % 8 == 0)) {
 #pragma unroll
@@ -313,15 +344,29 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int bidx, in
     for (int j = 0; j < 32; ++j)
       if (r == c0 + j) f[j] += p.gamma;
   }
-  uint32_t hp[16];
+  if (r >= p.M) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] = 0.f;
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const __half2 t = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
     hp[j] = *reinterpret_cast<const uint32_t*>(&t);
   }
-  // In symmetric mode an element is kept when r >= c (written) and mirrored
-  // when r > c.  `below`: every element of this warp's chunk is strictly below
-  // the diagonal (row0 is the warp's first row).
+}
+
+__device__ __forceinline__ uint16_t half_bits(const uint32_t (&hp)[16], int j) {
+  return static_cast<uint16_t>(hp[j / 2] >> (16 * (j % 2)));
+}
+
+// Element-wise stores of one chunk: chunks on the diagonal of a symmetric
+// result (an element is kept when r >= c and mirrored when r > c), or outputs
+// whose pitch a TMA map cannot describe.  row0 is the warp's first row.
+__device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx, int r, int c0, int row0,
+                                                   const uint32_t (&hp)[16]) {
+  if (r >= p.M) return;
+  const bool sym = p.mode == kSymLower;
+  const bool full = (c0 + 32 <= p.N);
   const bool below = !sym || (row0 > c0 + 31);
   __half* outb = p.out ? p.out + static_cast<long long>(bidx) * p.out_bs : nullptr;
   if (outb != nullptr) {
@@ -333,25 +378,23 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int bidx, in
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (c0 + j < p.N && (!sym || r >= c0 + j))
-          dst[j] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+        if (c0 + j < p.N && (!sym || r >= c0 + j)) dst[j] = __ushort_as_half(half_bits(hp, j));
     }
   }
   __half* tb = sym ? outb : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
   if (tb != nullptr) {
     const int ldt = sym ? p.ld_out : p.ld_outT;
-    // For a fixed column the warp's 32 lanes write 32 consecutive elements.
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int c = c0 + j;
-      if (c < p.N && (!sym || r > c))
-        tb[static_cast<size_t>(c) * ldt + r] = __ushort_as_half(static_cast<unsigned short>(hp[j / 2] >> (16 * (j % 2))));
+      if (c < p.N && (!sym || r > c)) tb[static_cast<size_t>(c) * ldt + r] = __ushort_as_half(half_bits(hp, j));
     }
   }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutT,
                         const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -359,12 +402,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + kStages * Smem::kABytes;
-  const uint32_t bar_full = base + Smem::kRingBytes;
+  const uint32_t staging = base + Smem::kRingBytes;
+  const uint32_t bar_full = staging + Smem::kStagingBytes;
   const uint32_t bar_empty = bar_full + kStages * 8;
   const uint32_t bar_tfull = bar_empty + kStages * 8;
   const uint32_t bar_tempty = bar_tfull + 2 * 8;
   const uint32_t bar_drain = bar_tempty + 2 * 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kBarBytes);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kStagingBytes + Smem::kBarBytes);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.K + BK - 1) / BK;
@@ -458,6 +503,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
+    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * Smem::kWarpStagingBytes;
+    const bool sym = p.mode == kSymLower;
+    // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
+    // of a symmetric result, or outT).
+    const bool want_n = p.out != nullptr;
+    const bool want_t = sym || p.outT != nullptr;
+    const bool tma_ok = (!want_n || p.tma_out) && (!want_t || (sym ? p.tma_out : p.tma_outT));
+    const CUtensorMap* map_t = sym ? &tmOut : &tmOutT;
+    uint32_t staged = 0;  // chunks this warp has staged (buffer rotation)
     uint32_t tc = 0;
     for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
       const int bidx = u / p.units_per_mat;
@@ -477,11 +531,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
-        epilogue_chunk(p, bidx, r, c0, row0, v);
+        // Warp-uniform classification of the chunk.
+        if (sym && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
+        if (row0 >= p.M) continue;            // rows out of range
+        uint32_t hp[16];
+        chunk_values(p, bidx, r, c0, v, hp);
+        if (!tma_ok || (sym && row0 <= c0 + 31)) {
+          store_chunk_scalar(p, bidx, r, c0, row0, hp);
+          continue;
+        }
+        // Stage the box (and its transpose) in swizzled shared memory, then
+        // one lane writes them with bulk tensor stores.
+        const uint32_t buf = my_staging + (staged & 1u) * (2 * Smem::kStageBoxBytes);
+        if (lane == 0 && staged >= 2) bulk_wait_read_1();
+        __syncwarp();
+        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+        if (want_n) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
+                         hp[4 * q + 2], hp[4 * q + 3]);
+        }
+        if (want_t) {
+          const uint32_t tbuf = buf + Smem::kStageBoxBytes;
+          const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
+        }
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
+          if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
+          bulk_commit();
+        }
+        ++staged;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(bar_tempty + 8 * acc, 0));
     }
+    // Every bulk store has finished before the CTA (and its shared memory)
+    // goes away.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   // Neither CTA leaves while its peer may still multicast into its shared
@@ -508,6 +601,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(q_fn);
   });
   return fn;
+}
+
+// 3-D tensor map over [batch][rows][cols] fp16 for the epilogue's bulk
+// stores: box 32 x 32 x 1 with the 64-byte swizzle of the staging buffers.
+bool make_store_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, int rows, int cols,
+                    int batch) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, static_cast<cuuint64_t>(bstride) * 2u};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// An output can take the bulk-store path when its base is 16-byte aligned and
+// its row pitch and batch stride are multiples of 8 elements.
+bool storable(const __half* ptr, int ld, long long bstride, int rows, int batch) {
+  if (ptr == nullptr) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0 || ld % 8 != 0 || bstride % 8 != 0) return false;
+  return batch == 1 || bstride >= static_cast<long long>(ld) * rows;
 }
 
 // 3-D tensor map over [batch][rows][cols] fp16 with row pitch `ld` elements,
@@ -582,6 +700,19 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2)) return cudaErrorInvalidValue;
 
+  CUtensorMap to, tt;
+  memset(&to, 0, sizeof to);
+  memset(&tt, 0, sizeof tt);
+  int tma_out = 0, tma_outT = 0;
+  if (storable(g.out, g.ld_out, g.out_bstride, g.M, g.batch) &&
+      make_store_map(&to, g.out, g.out_bstride > 0 ? g.out_bstride : static_cast<long long>(g.ld_out) * g.M,
+                     g.ld_out, g.M, g.N, g.batch))
+    tma_out = 1;
+  if (g.mode == kRect && storable(g.outT, g.ld_outT, g.outT_bstride, g.N, g.batch) &&
+      make_store_map(&tt, g.outT, g.outT_bstride > 0 ? g.outT_bstride : static_cast<long long>(g.ld_outT) * g.N,
+                     g.ld_outT, g.N, g.M, g.batch))
+    tma_outT = 1;
+
   GemmParams p{};
   p.M = g.M;
   p.N = g.N;
@@ -611,11 +742,13 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.outT = g.outT;
   p.outT_bs = g.outT_bstride;
   p.ld_outT = g.ld_outT;
+  p.tma_out = tma_out;
+  p.tma_outT = tma_outT;
   p.status = dev_status;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;
-  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, p);
+  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, to, tt, p);
   return cudaGetLastError();
 }
 

@@ -248,76 +248,54 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
   for (int p = 0; p < a.fro2_parts; ++p) f2 += a.fro2[static_cast<size_t>(b) * a.fro2_parts + p];
   const float inv = 1.0f / (sqrtf(f2) + a.eps);
 
-  // Each warp handles rows warp, warp + 8, warp + 16, warp + 24 of the tile.
-  // All four row segments are loaded before any store, so four independent
-  // 16-byte loads per thread are in flight (the decay stores could alias the
-  // next row's loads, which would otherwise serialise them).
-  constexpr int kRowsPerWarp = kGRows / (256 / kWarp);
-  const int c = c0 + lane * 4;
-  const bool full = VEC && (c + 4 <= a.m);
-  float v[kRowsPerWarp][4];
-  bool live[kRowsPerWarp];
-  float* srcp[kRowsPerWarp];
-#pragma unroll
-  for (int q = 0; q < kRowsPerWarp; ++q) {
-    const int i = i0 + warp + q * (256 / kWarp);
-    live[q] = i < a.k && c < a.m;
-    srcp[q] = nullptr;
-    v[q][0] = v[q][1] = v[q][2] = v[q][3] = 0.f;
+  for (int rr = warp; rr < kGRows; rr += 256 / kWarp) {
+    const int i = i0 + rr;
+    const int c = c0 + lane * 4;
+    __half h[4] = {__float2half_rn(0.f), __float2half_rn(0.f), __float2half_rn(0.f), __float2half_rn(0.f)};
+    bool live = i < a.k && c < a.m;
+    int row = 0;
     if constexpr (SRC_F32) {
       if (i < a.k) {
-        const int row = a.idx[static_cast<size_t>(b) * a.k + i];
+        row = a.idx[static_cast<size_t>(b) * a.k + i];
         if (row < 0 || row >= a.n) {  // never expected: record it and skip the access
           if (lane == 0) atomicOr(a.status, kDevCheck);
-          live[q] = false;
-        } else {
-          srcp[q] = a.M[b] + static_cast<size_t>(row) * a.m;
+          live = false;
         }
       }
-      if (live[q]) {
+    }
+    if (live) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool full = VEC && (c + 4 <= a.m);
+      if constexpr (SRC_F32) {
+        float* src = a.M[b] + static_cast<size_t>(row) * a.m;
         if (full) {
-          const float4 x = *reinterpret_cast<const float4*>(srcp[q] + c);
-          v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
+          const float4 x = *reinterpret_cast<const float4*>(src + c);
+          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+          if (a.decay)
+            *reinterpret_cast<float4*>(src + c) =
+                make_float4(__fmul_rn(a.mu, x.x), __fmul_rn(a.mu, x.y), __fmul_rn(a.mu, x.z), __fmul_rn(a.mu, x.w));
         } else {
           for (int j = 0; j < 4; ++j)
-            if (c + j < a.m) v[q][j] = srcp[q][c + j];
+            if (c + j < a.m) {
+              v[j] = src[c + j];
+              if (a.decay) src[c + j] = __fmul_rn(a.mu, v[j]);
+            }
         }
-      }
-    } else {
-      if (live[q]) {
+      } else {
         const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * a.m;
         if (full) {
           const uint2 x = *reinterpret_cast<const uint2*>(src + c);
           const __half2 p0 = *reinterpret_cast<const __half2*>(&x.x);
           const __half2 p1 = *reinterpret_cast<const __half2*>(&x.y);
-          v[q][0] = __low2float(p0); v[q][1] = __high2float(p0);
-          v[q][2] = __low2float(p1); v[q][3] = __high2float(p1);
+          v[0] = __low2float(p0); v[1] = __high2float(p0);
+          v[2] = __low2float(p1); v[3] = __high2float(p1);
         } else {
           for (int j = 0; j < 4; ++j)
-            if (c + j < a.m) v[q][j] = __half2float(src[c + j]);
+            if (c + j < a.m) v[j] = __half2float(src[c + j]);
         }
       }
-    }
-  }
 #pragma unroll
-  for (int q = 0; q < kRowsPerWarp; ++q) {
-    const int rr = warp + q * (256 / kWarp);
-    const int i = i0 + rr;
-    __half h[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) h[j] = __float2half_rn(live[q] ? v[q][j] * inv : 0.f);
-    if (live[q]) {
-      if constexpr (SRC_F32) {
-        if (a.decay) {
-          if (full) {
-            *reinterpret_cast<float4*>(srcp[q] + c) = make_float4(
-                __fmul_rn(a.mu, v[q][0]), __fmul_rn(a.mu, v[q][1]), __fmul_rn(a.mu, v[q][2]), __fmul_rn(a.mu, v[q][3]));
-          } else {
-            for (int j = 0; j < 4; ++j)
-              if (c + j < a.m) srcp[q][c + j] = __fmul_rn(a.mu, v[q][j]);
-          }
-        }
-      }
+      for (int j = 0; j < 4; ++j) h[j] = __float2half_rn(v[j] * inv);
       __half* dst = a.out_rows + static_cast<long long>(b) * a.rows_bstride + static_cast<size_t>(i) * a.ld_rows + c;
       if (full && (a.ld_rows % 4 == 0)) {
         uint2 w;
