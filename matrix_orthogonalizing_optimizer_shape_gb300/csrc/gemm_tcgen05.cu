@@ -33,9 +33,13 @@
 //                  even CTA lane 0 issues the paired MMAs into one of two
 //                  256-column fp32 accumulators and releases ring slots and
 //                  accumulators in both CTAs with multicast commits;
-//   warps 2..5     epilogue (both CTAs): tcgen05.ld of the 32 TMEM lanes each
-//                  warp may access (warp % 4), alpha/beta/gamma, fp16 stores;
-//                  then they tell the even CTA that the accumulator is free.
+//   warps 2..9     epilogue (both CTAs): two warps per TMEM lane quadrant
+//                  (warp % 4), each taking half of the 256 columns, 32 at a
+//                  time: tcgen05.ld, alpha/beta/gamma, then the 32 x 32 box
+//                  (and its transpose) staged in swizzled shared memory and
+//                  written with bulk tensor stores (chunks on the diagonal of
+//                  a symmetric result are written element by element); then
+//                  they tell the even CTA that the accumulator is free.
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that runs out sets a bit in the device status word and the CTA winds down:
 // the issuing CTA waits (bounded) for its MMAs, both CTAs meet at a cluster
@@ -56,7 +60,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // fp16 elements per 128-byte swizzle row
 constexpr int BN = 256;
 constexpr int kStages = 6;
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, each half of the columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
@@ -153,8 +158,8 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// At most one of this thread's bulk groups may still be reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// None of this thread's bulk groups is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Generic-proxy shared-memory writes become visible to the async proxy.
 __device__ __forceinline__ void fence_async_shared() {
@@ -298,12 +303,12 @@ struct Smem {
   static constexpr int kBBytes = (BN / 2) * BK * 2;   // this CTA's half of B: 16 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  // Epilogue staging: per epilogue warp two buffers, each a 32 x 32 fp16 box
-  // and its transpose (2 KB each), laid out with the 64-byte swizzle of the
-  // store tensor maps.
+  // Epilogue staging: per epilogue warp one 32 x 32 fp16 box and its
+  // transpose (2 KB each), laid out with the 64-byte swizzle of the store
+  // tensor maps.
   static constexpr int kStageBoxBytes = 32 * 32 * 2;
-  static constexpr int kWarpStagingBytes = 2 * 2 * kStageBoxBytes;
-  static constexpr int kStagingBytes = 4 * kWarpStagingBytes;
+  static constexpr int kWarpStagingBytes = 2 * kStageBoxBytes;
+  static constexpr int kStagingBytes = kEpiWarps * kWarpStagingBytes;
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int kBarBytes = (2 * kStages + 5) * 8;
   static constexpr int kDyn = 1024 + kRingBytes + kStagingBytes + kBarBytes + 16;
@@ -313,18 +318,31 @@ struct Smem {
 // row r; v[j] is column c0 + j of the fp32 accumulator.  hp receives
 // alpha D + beta C + gamma I as packed fp16 pairs (rows r >= M give zeros and
 // read nothing).
+// The C operand of a chunk in 16-byte pieces, loaded before the TMEM read so
+// the two latencies overlap (only when the chunk is full and C's pitch allows
+// vector loads; otherwise chunk_values reads C element-wise).
+__device__ __forceinline__ bool c_vector_ok(const GemmParams& p, int c0) {
+  return p.C != nullptr && (c0 + 32 <= p.N) && (p.ldc % 8 == 0);
+}
+__device__ __forceinline__ void prefetch_c(const GemmParams& p, int bidx, int r, int c0, uint4 (&cv)[4]) {
+  if (c_vector_ok(p, c0) && r < p.M) {
+    const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cv[q] = *reinterpret_cast<const uint4*>(crow + 8 * q);
+  }
+}
+
 __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
-                                             uint32_t (&hp)[16]) {
-  const bool full = (c0 + 32 <= p.N);
+                                             const uint4 (&cv)[4], uint32_t (&hp)[16]) {
   float f[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
   if (p.C != nullptr && r < p.M) {
     const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
-    if (full && (p.ldc % 8 == 0)) {
+    if (c_vector_ok(p, c0)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(crow + 8 * q);
+        const uint4 u = cv[q];
         const __half2* h2 = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -425,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, 256);  // used in the even CTA: both CTAs' epilogue threads
+      mbar_init(bar_tempty + 8 * a, 2 * 32 * kEpiWarps);  // used in the even CTA: both CTAs' epilogue threads
     }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
@@ -501,8 +519,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(bar_drain, 0u, p.status);
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2 .. 2 + kEpiWarps - 1 ----------------
     const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
+    const int col_lo = ((warp - 2) / 4) * (BN * 4 / kEpiWarps);  // this warp's columns of the tile
+    const int col_hi = col_lo + BN * 4 / kEpiWarps;
     const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * Smem::kWarpStagingBytes;
     const bool sym = p.mode == kSymLower;
     // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
@@ -511,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool want_t = sym || p.outT != nullptr;
     const bool tma_ok = (!want_n || p.tma_out) && (!want_t || (sym ? p.tma_out : p.tma_outT));
     const CUtensorMap* map_t = sym ? &tmOut : &tmOutT;
-    uint32_t staged = 0;  // chunks this warp has staged (buffer rotation)
+    uint32_t staged = 0;  // chunks this warp has staged
     uint32_t tc = 0;
     for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
       const int bidx = u / p.units_per_mat;
@@ -525,25 +545,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
-      for (int cc = 0; cc < BN; cc += 32) {
+      for (int cc = col_lo; cc < col_hi; cc += 32) {
         const int c0 = bc * BN + cc;
-        if (c0 >= p.N) break;  // uniform across the CTA
+        // Warp-uniform classification of the chunk.
+        if (c0 >= p.N) break;
+        if (sym && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
+        if (row0 >= p.M) continue;            // rows out of range
+        uint4 cv[4];
+        prefetch_c(p, bidx, r, c0, cv);
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
-        // Warp-uniform classification of the chunk.
-        if (sym && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
-        if (row0 >= p.M) continue;            // rows out of range
         uint32_t hp[16];
-        chunk_values(p, bidx, r, c0, v, hp);
+        chunk_values(p, bidx, r, c0, v, cv, hp);
         if (!tma_ok || (sym && row0 <= c0 + 31)) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp);
           continue;
         }
         // Stage the box (and its transpose) in swizzled shared memory, then
         // one lane writes them with bulk tensor stores.
-        const uint32_t buf = my_staging + (staged & 1u) * (2 * Smem::kStageBoxBytes);
-        if (lane == 0 && staged >= 2) bulk_wait_read_1();
+        const uint32_t buf = my_staging;
+        if (lane == 0 && staged >= 1) bulk_wait_read_0();
         __syncwarp();
         const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
         if (want_n) {
