@@ -65,7 +65,7 @@ dion3_status ok() {
 // FLOPs for the GEMM, bytes for the memory-bound kernels).
 // ---------------------------------------------------------------------------
 struct TraceRec {
-  const char* name;
+  std::string name;
   cudaEvent_t a, b;
   double flops, bytes;
 };
@@ -94,7 +94,7 @@ void trace_clear_locked() {
 }
 
 template <class Launch>
-cudaError_t traced(const char* name, double flops, double bytes, cudaStream_t s, Launch&& launch) {
+cudaError_t traced(const std::string& name, double flops, double bytes, cudaStream_t s, Launch&& launch) {
   std::unique_lock<std::mutex> lock(g_trace_mu);
   if (!g_trace_on) {
     lock.unlock();
@@ -214,12 +214,13 @@ cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
   const double flops = g.mode == kSymLower ? static_cast<double>(g.M) * g.M * g.K * g.batch
                                            : 2.0 * g.M * g.N * g.K * g.batch;
   const double bytes = 2.0 * g.batch * (static_cast<double>(g.M) * g.K + static_cast<double>(g.N) * g.K);
-  static const bool detail = [] {
+  static const int detail = [] {
     const char* v = getenv("DION3_TRACE_DETAIL");
-    return v != nullptr && v[0] == '1';
+    return v != nullptr ? atoi(v) : 0;
   }();
-  const char* name = "gemm_tcgen05";
-  if (detail) name = g.mode == kRect ? "gemm_tcgen05:rect" : (g.K == g.M ? "gemm_tcgen05:sym_square" : "gemm_tcgen05:syrk");
+  std::string name = "gemm_tcgen05";
+  if (detail >= 1) name = g.mode == kRect ? "gemm:rect" : (g.K == g.M ? "gemm:sym_square" : "gemm:syrk");
+  if (detail >= 2) name += ":" + std::to_string(g.mode == kRect ? g.N : g.M);
   return traced(name, flops, bytes, s, [&] { return launch_gemm(g, st, s); });
 }
 cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
@@ -298,7 +299,11 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     g.out = D; g.out_bstride = p.s_bs; g.ld_out = p.sp;
     return g;
   };
-  auto launch = [&](const GemmDesc& g) -> dion3_status {
+  bool reverse = false;  // serpentine batch order across the chain
+  auto launch = [&](const GemmDesc& g0) -> dion3_status {
+    GemmDesc g = g0;
+    g.reverse = reverse;
+    reverse = !reverse;
     const char* why = nullptr;
     if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
     const cudaError_t e = traced_gemm(g, st, stream);
@@ -887,11 +892,11 @@ dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32
     if ((e = cudaEventElapsedTime(&ms, r.a, r.b)) != cudaSuccess) return cuda_fail(e, "trace elapsed time");
     dion3_trace_entry* slot = nullptr;
     for (auto& x : agg)
-      if (strncmp(x.name, r.name, sizeof x.name) == 0) slot = &x;
+      if (strncmp(x.name, r.name.c_str(), sizeof x.name - 1) == 0) slot = &x;
     if (slot == nullptr) {
       agg.push_back(dion3_trace_entry{});
       slot = &agg.back();
-      snprintf(slot->name, sizeof slot->name, "%s", r.name);
+      snprintf(slot->name, sizeof slot->name, "%s", r.name.c_str());
     }
     slot->launches += 1;
     slot->total_ms += ms;

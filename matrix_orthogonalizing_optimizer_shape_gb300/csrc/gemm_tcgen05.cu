@@ -75,6 +75,7 @@ struct GemmParams {
   __half* out; long long out_bs; int ld_out;
   __half* outT; long long outT_bs; int ld_outT;
   int tma_out, tma_outT;     // the output has a TMA store map (16-byte pitch rules hold)
+  int batch, reverse;        // visit matrices from the last one when reverse
   unsigned* status;
 };
 
@@ -462,7 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t kc = 0;
       bool ok = true;
       for (int u = cluster; u < p.total_units && ok; u += nclusters) {
-        const int bidx = u / p.units_per_mat;
+        const int bidx = p.reverse ? p.batch - 1 - u / p.units_per_mat : u / p.units_per_mat;
         int P, bc;
         unit_coords(p, u % p.units_per_mat, P, bc);
         const int bi = 2 * P + static_cast<int>(rank);
@@ -534,7 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t staged = 0;  // chunks this warp has staged
     uint32_t tc = 0;
     for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
-      const int bidx = u / p.units_per_mat;
+      const int bidx = p.reverse ? p.batch - 1 - u / p.units_per_mat : u / p.units_per_mat;
       int P, bc;
       unit_coords(p, u % p.units_per_mat, P, bc);
       const int bi = 2 * P + static_cast<int>(rank);
@@ -766,6 +767,8 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.ld_outT = g.ld_outT;
   p.tma_out = tma_out;
   p.tma_outT = tma_outT;
+  p.batch = g.batch;
+  p.reverse = g.reverse ? 1 : 0;
   p.status = dev_status;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));

@@ -97,6 +97,10 @@ struct GemmDesc {
   const __half* C; long long c_bstride; int ldc;     // may be null (beta ignored)
   __half* out; long long out_bstride; int ld_out;    // may be null in kRect
   __half* outT; long long outT_bstride; int ld_outT; // may be null
+  // Visit the batch from the last matrix to the first.  Consecutive launches
+  // of a chain alternate the order, so each starts on the matrices the
+  // previous one wrote last (still in L2).
+  bool reverse = false;
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA
