@@ -111,3 +111,14 @@ def test_step_ragged_groups(cuda_lib, f):
     hp = d3.HParams(f=f, mu=0.9, lr=0.01)
     for _ in range(2):
         _step_and_compare(mats, grads, hp)
+
+
+@pytest.mark.parametrize("n,m,f", [(40, 64, 0.01), (64, 1, 0.5), (1, 48, 1.0), (33, 7, 1.0), (8, 8, 1.0)])
+def test_step_degenerate_shapes(cuda_lib, n, m, f):
+    # k = 1 (one selected row), m = 1 (Gram side 1 on the transpose), n = 1,
+    # tiny ragged and square cases.
+    M = workloads.gapped_momentum(n, m, seed=n + m) if n > 1 else workloads.gaussian((n, m), 1.0, 5)
+    W = workloads.gaussian((n, m), 0.02, seed=6, dtype="bf16")
+    G = workloads.gaussian((n, m), 0.01, seed=7, dtype="bf16")
+    mat = Mat(W, M, "bf16", "bf16")
+    _step_and_compare([[mat]], [[G]], d3.HParams(f=f, mu=0.9, lr=0.01))
