@@ -151,6 +151,34 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank helpers (one process per GPU; the unit of work, one matrix, is
+# independent, so ranks share nothing on the data path: weak scaling).
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest
+    rank's); `device` is where the reduction tensor lives (cuda for NCCL,
+    cpu for gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job useful TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
+def rank_barrier(world: int):
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 
@@ -217,8 +245,7 @@ def run_ours(args, rank, world, device_index):
     stream = torch.cuda.current_stream(device)
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
 
     for _ in range(args.warmup):
         d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
@@ -242,11 +269,7 @@ def run_ours(args, rank, world, device_index):
     d3.trace_enable(False)
     d3.device_status(stream)
     ms = ev0.elapsed_time(ev1) / args.steps
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, device)
     launches = sum(v["launches"] for v in trace.values())
 
     # End to end: every step copies its gradients from pinned host memory and
@@ -305,12 +328,8 @@ def run_ours(args, rank, world, device_index):
         e1.record(stream)
         torch.cuda.synchronize(device)
         barrier()
-        ems = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * flops_rank / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+        e2e = {"value": job_tflops(flops_rank, world, ems), "unit": "TFLOP/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "method": f"pinned host gradients copied on a side stream in sub-batches of <= {chunk} "
                          "matrices, each sub-batch stepped as soon as it lands; selected rows read back",
@@ -348,7 +367,7 @@ def run_ours(args, rank, world, device_index):
             kv["gbs"] = v["algo_bytes"] / (v["total_ms"] * 1e-3) / 1e9
         kernels[name] = kv
 
-    value = world * flops_rank / (ms_max * 1e-3) / 1e12
+    value = job_tflops(flops_rank, world, ms_max)
     bf16_peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
