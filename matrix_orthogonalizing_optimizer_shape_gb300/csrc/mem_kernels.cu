@@ -238,7 +238,10 @@ constexpr int kGRows = 32, kGCols = 128;
 
 template <bool SRC_F32, bool VEC>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherArgs a) {
-  __shared__ __align__(16) __half tile[kGCols][kGRows + 8];
+  // Column-major staging: a pitch of 34 halves (17 words) spreads the 2-byte
+  // writes of a warp over 8 banks (4-way conflicts; a 16-byte-aligned pitch of
+  // 40 gave 16-way conflicts and cost a quarter of the kernel's time).
+  __shared__ __align__(16) __half tile[kGCols][kGRows + 2];
   const int b = blockIdx.z;
   const int i0 = blockIdx.y * kGRows;
   const int c0 = blockIdx.x * kGCols;
@@ -324,7 +327,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     if (c >= a.m || i >= a.ld_cols) continue;
     __half* dst = a.out_cols + static_cast<long long>(b) * a.cols_bstride + static_cast<size_t>(c) * a.ld_cols + i;
     if (i + 8 <= a.ld_cols && (a.ld_cols % 8 == 0)) {
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[cc][seg]);
+      const uint32_t* t32 = reinterpret_cast<const uint32_t*>(&tile[cc][seg]);  // 4-byte aligned rows
+      *reinterpret_cast<uint4*>(dst) = make_uint4(t32[0], t32[1], t32[2], t32[3]);
     } else {
       for (int j = 0; j < 8 && i + j < a.ld_cols; ++j) dst[j] = tile[cc][seg + j];
     }
