@@ -242,6 +242,11 @@ cudaError_t traced_sumsq(const __half* X, long long n, int batch, float* parts, 
   return traced("sumsq_f16", 0.0, 2.0 * n * batch, s,
                 [&] { return launch_sumsq_f16(X, n, batch, parts, nparts, s); });
 }
+cudaError_t traced_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
+  const double pb = a.param_dtype == kBF16 ? 2.0 : 4.0;
+  const double bytes = static_cast<double>(a.batch) * a.k * a.cols * (2.0 + 2.0 * pb);
+  return traced("scatter_update", 0.0, bytes, s, [&] { return launch_scatter(a, vec, s); });
+}
 
 // Useful FLOPs of the schedule run_gram_ns() launches (triangle = half).
 double schedule_flops(int k, int m, const dion3_hparams& hp) {
@@ -275,14 +280,6 @@ struct NsOut {
   __half* O;
   long long o_bs;
   int ld_o;
-  // Fused row-scatter update (dion3_step): when set, the final multiply-back
-  // applies W[S] <- round_p(W[S] - lr_eff O) in its epilogue and O is not
-  // written.
-  bool update = false;
-  void* const* W = nullptr;  // host array [batch] of parameter pointers
-  int w_dtype = 0, w_cols = 0, w_rows = 0;
-  const int32_t* idx = nullptr;  // [batch][k]
-  float neg_lr = 0.f;
 };
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
@@ -359,30 +356,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
       if ((rc = launch(sym(p.S[Z], p.S[tm], p.S[R], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
     }
   }
-  // O = Q Y, written as X's k x m orientation, or applied to W directly.
-  if (out.update) {
-    for (int b0 = 0; b0 < p.batch; b0 += kMaxUpdateBatch) {
-      const int nb = std::min(kMaxUpdateBatch, p.batch - b0);
-      GemmUpdate u{};
-      u.enabled = 1;
-      u.tall = p.wide ? 0 : 1;
-      u.w_dtype = out.w_dtype;
-      u.w_cols = out.w_cols;
-      u.w_rows = out.w_rows;
-      u.k = p.k;
-      u.idx = out.idx + static_cast<size_t>(b0) * p.k;
-      u.neg_lr = out.neg_lr;
-      for (int i = 0; i < nb; ++i) u.W[i] = out.W[b0 + i];
-      GemmDesc g{};
-      g.A = p.Yt[ycur] + p.yt_bs * b0; g.a_bstride = p.yt_bs; g.lda = p.sp;
-      g.B = p.S[Q] + p.s_bs * b0; g.b_bstride = p.s_bs; g.ldb = p.sp;
-      g.M = p.L; g.N = p.s; g.K = p.s; g.batch = nb;
-      g.mode = kRect; g.alpha = 1.f;
-      g.update = &u;
-      if ((rc = launch(g)) != DION3_OK) return rc;
-    }
-    return DION3_OK;
-  }
+  // O = Q Y, written as X's k x m orientation.
   GemmDesc g{};
   g.A = p.Yt[ycur]; g.a_bstride = p.yt_bs; g.lda = p.sp;
   g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
@@ -517,6 +491,9 @@ struct GroupPlan {
   float* sq;
   int32_t* idx;
   float* fro2;
+  __half* O;
+  long long o_bs;
+  int ld_o;
   NsPlan ns;
 };
 
@@ -529,6 +506,9 @@ void plan_group(Carver& c, const dion3_group& g, float f, GroupPlan& gp) {
   gp.sq = c.take<float>(static_cast<long long>(g.batch) * g.rows);
   gp.idx = c.take<int32_t>(static_cast<long long>(g.batch) * gp.k);
   gp.fro2 = c.take<float>(g.batch);
+  gp.ld_o = static_cast<int>(round_up(g.cols, 8));
+  gp.o_bs = static_cast<long long>(gp.k) * gp.ld_o;
+  gp.O = c.take<__half>(gp.o_bs * g.batch);
   plan_ns(c, gp.k, gp.m, gp.batch, gp.ns);
 }
 
@@ -838,17 +818,20 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       ga.out_cols += ga.cols_bstride * b0;
       if ((e = traced_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
     }
-    // (b) + (c): Gram NS; its final multiply-back applies the row-scatter
-    // update W[S] <- round_p(W[S] - (lr / sqrt f) O) in the GEMM epilogue.
-    NsOut out{nullptr, 0, 0};
-    out.update = true;
-    out.W = g.params;
-    out.w_dtype = g.param_dtype == DION3_BF16 ? kBF16 : kF32;
-    out.w_cols = g.cols;
-    out.w_rows = g.rows;
-    out.idx = idx;
-    out.neg_lr = -lr_eff;
+    NsOut out{gp.O, gp.o_bs, gp.ld_o};
     if ((rc = run_gram_ns(gp.ns, *hp, out, st, s)) != DION3_OK) return rc;
+    // (c) scatter update of the selected parameter rows.
+    for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
+      const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
+      ScatterArgs sa{};
+      sa.rows = g.rows; sa.cols = g.cols; sa.k = gp.k; sa.batch = nb; sa.param_dtype = g.param_dtype;
+      for (int i = 0; i < nb; ++i) sa.W[i] = g.params[b0 + i];
+      sa.idx = idx + static_cast<size_t>(b0) * gp.k;
+      sa.O = gp.O + gp.o_bs * b0; sa.o_bstride = gp.o_bs; sa.ld_o = gp.ld_o;
+      sa.lr = lr_eff;
+      sa.status = st;
+      if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
+    }
   }
   return ok();
 }

@@ -48,7 +48,6 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -412,134 +411,10 @@ __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx
   }
 }
 
-// Fused row-scatter update of one 32 x 32 accumulator chunk (the final
-// multiply-back O = Q Y of a Dion3 step): W[S_i] <- round_p(W[S_i] - lr O_i)
-// straight from the fp32 accumulator (alpha = 1, no C).  Thread `lane` holds
-// row r of the chunk; row0 is the warp's first row, c0 the first column.
-//   tall:  D = O (rows = selected rows i, columns = W columns): each thread
-//          updates 32 consecutive elements of W[S_r];
-//   wide:  D = O^T (rows = W columns, columns = selected rows): the chunk is
-//          staged through shared memory (fp32, 4 KB) so that 8 lanes update
-//          one 32-element W row segment.
-// Selected indices are checked against the W row count (a bad one sets the
-// device status word and is skipped).
-__device__ __forceinline__ void update_chunk(const GemmParams& p, const GemmUpdate& u, int bidx, int r, int row0,
-                                             int c0, const uint32_t (&v)[32], uint32_t staging, int lane) {
-  const float nlr = u.neg_lr;
-  if (u.tall) {
-    if (r >= p.M) return;
-    const int row = u.idx[static_cast<size_t>(bidx) * u.k + r];
-    if (row < 0 || row >= u.w_rows) {
-      atomicOr(p.status, kDevCheck);
-      return;
-    }
-    const bool full = c0 + 32 <= p.N;
-    if (u.w_dtype == kBF16) {
-      __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(u.W[bidx]) + static_cast<size_t>(row) * u.w_cols + c0;
-      if (full && (u.w_cols % 8 == 0)) {
-        uint4 x[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) x[q] = *reinterpret_cast<const uint4*>(w + 8 * q);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t wd[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 8 * q + 2 * e;
-            const float lo = __uint_as_float(wd[e] << 16), hi = __uint_as_float(wd[e] & 0xffff0000u);
-            const __nv_bfloat162 t = __floats2bfloat162_rn(fmaf(nlr, __uint_as_float(v[j]), lo),
-                                                           fmaf(nlr, __uint_as_float(v[j + 1]), hi));
-            wd[e] = *reinterpret_cast<const uint32_t*>(&t);
-          }
-          *reinterpret_cast<uint4*>(w + 8 * q) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        }
-      } else {
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < p.N) w[j] = __float2bfloat16_rn(fmaf(nlr, __uint_as_float(v[j]), __bfloat162float(w[j])));
-      }
-    } else {
-      float* w = reinterpret_cast<float*>(u.W[bidx]) + static_cast<size_t>(row) * u.w_cols + c0;
-      if (full && (u.w_cols % 4 == 0)) {
-        float4 x[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = *reinterpret_cast<const float4*>(w + 4 * q);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          x[q].x = fmaf(nlr, __uint_as_float(v[4 * q]), x[q].x);
-          x[q].y = fmaf(nlr, __uint_as_float(v[4 * q + 1]), x[q].y);
-          x[q].z = fmaf(nlr, __uint_as_float(v[4 * q + 2]), x[q].z);
-          x[q].w = fmaf(nlr, __uint_as_float(v[4 * q + 3]), x[q].w);
-          *reinterpret_cast<float4*>(w + 4 * q) = x[q];
-        }
-      } else {
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < p.N) w[j] = fmaf(nlr, __uint_as_float(v[j]), w[j]);
-      }
-    }
-    return;
-  }
-  // wide: stage the chunk as fp32 [32 columns c][32 rows r] (4 KB), then 8 lanes
-  // per W row segment.
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(staging + static_cast<uint32_t>((j * 32 + lane) * 4)), "r"(v[j])
-                 : "memory");
-  __syncwarp();
-  const int ro = (lane % 8) * 4;  // row offset within the chunk (W column offset)
-#pragma unroll 1
-  for (int it = 0; it < 8; ++it) {
-    const int cr = it * 4 + lane / 8;  // chunk column: selected row c0 + cr
-    const int c = c0 + cr;
-    const int rr = row0 + ro;          // first W column of this lane
-    if (c >= p.N || rr >= p.M) continue;
-    const int row = u.idx[static_cast<size_t>(bidx) * u.k + c];
-    if (row < 0 || row >= u.w_rows) {
-      atomicOr(p.status, kDevCheck);
-      continue;
-    }
-    float val[4];
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(val[0]), "=f"(val[1]), "=f"(val[2]), "=f"(val[3])
-                 : "r"(staging + static_cast<uint32_t>((cr * 32 + ro) * 4)));
-    const bool full4 = rr + 4 <= p.M;
-    if (u.w_dtype == kBF16) {
-      __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(u.W[bidx]) + static_cast<size_t>(row) * u.w_cols + rr;
-      if (full4 && (u.w_cols % 4 == 0)) {
-        uint2 x = *reinterpret_cast<const uint2*>(w);
-        const __nv_bfloat162 t0 = __floats2bfloat162_rn(fmaf(nlr, val[0], __uint_as_float(x.x << 16)),
-                                                        fmaf(nlr, val[1], __uint_as_float(x.x & 0xffff0000u)));
-        const __nv_bfloat162 t1 = __floats2bfloat162_rn(fmaf(nlr, val[2], __uint_as_float(x.y << 16)),
-                                                        fmaf(nlr, val[3], __uint_as_float(x.y & 0xffff0000u)));
-        x.x = *reinterpret_cast<const uint32_t*>(&t0);
-        x.y = *reinterpret_cast<const uint32_t*>(&t1);
-        *reinterpret_cast<uint2*>(w) = x;
-      } else {
-        for (int e = 0; e < 4; ++e)
-          if (rr + e < p.M) w[e] = __float2bfloat16_rn(fmaf(nlr, val[e], __bfloat162float(w[e])));
-      }
-    } else {
-      float* w = reinterpret_cast<float*>(u.W[bidx]) + static_cast<size_t>(row) * u.w_cols + rr;
-      if (full4 && (u.w_cols % 4 == 0)) {
-        float4 x = *reinterpret_cast<const float4*>(w);
-        x.x = fmaf(nlr, val[0], x.x);
-        x.y = fmaf(nlr, val[1], x.y);
-        x.z = fmaf(nlr, val[2], x.z);
-        x.w = fmaf(nlr, val[3], x.w);
-        *reinterpret_cast<float4*>(w) = x;
-      } else {
-        for (int e = 0; e < 4; ++e)
-          if (rr + e < p.M) w[e] = fmaf(nlr, val[e], w[e]);
-      }
-    }
-  }
-  __syncwarp();
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutT,
-                        const __grid_constant__ GemmParams p, const __grid_constant__ GemmUpdate upd) {
+                        const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -682,10 +557,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
-        if (upd.enabled) {
-          update_chunk(p, upd, bidx, r, row0, c0, v, my_staging, lane);
-          continue;
-        }
         uint32_t hp[16];
         chunk_values(p, bidx, r, c0, v, cv, hp);
         if (!tma_ok || (sym && row0 <= c0 + 31)) {
@@ -832,9 +703,7 @@ bool gemm_check(const GemmDesc& g, const char** why) {
     return fail("gemm: operand pitches must be multiples of 8 elements");
   if (g.lda < g.K || g.ldb < g.K) return fail("gemm: pitch smaller than K");
   if (g.mode == kSymLower && (g.M != g.N || g.out == nullptr)) return fail("gemm: symmetric mode needs M == N and out");
-  if (g.mode == kRect && g.out == nullptr && g.outT == nullptr && g.update == nullptr) return fail("gemm: no output");
-  if (g.update != nullptr && (g.mode != kRect || g.batch > kMaxUpdateBatch || g.C != nullptr || g.alpha != 1.0f))
-    return fail("gemm: fused update needs a rectangular product, alpha 1, no C and <= 256 matrices");
+  if (g.mode == kRect && g.out == nullptr && g.outT == nullptr) return fail("gemm: no output");
   if (g.M > (1 << 24) || g.N > (1 << 24)) return fail("gemm: dimension too large");
   return true;
 }
@@ -904,9 +773,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;
-  GemmUpdate u{};
-  if (g.update != nullptr) u = *g.update;
-  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, to, tt, p, u);
+  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, to, tt, p);
   return cudaGetLastError();
 }
 

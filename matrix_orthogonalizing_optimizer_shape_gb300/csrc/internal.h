@@ -66,6 +66,17 @@ cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s);
 cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts,
                              int nparts, cudaStream_t s);
 
+// a7: W[S_i] <- round(W[S_i] - lr O[i]) for the selected rows.
+struct ScatterArgs {
+  int rows, cols, k, batch;        // batch <= kMaxBatchPerLaunch
+  int param_dtype;                 // kF32 or kBF16
+  void* W[kMaxBatchPerLaunch];
+  const int32_t* idx;              // [batch][k]
+  const __half* O; long long o_bstride; int ld_o;   // [k][ld_o]
+  float lr;
+  unsigned* status;                // device status word (kDevCheck on a bad index)
+};
+cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Tensor-core GEMM (gemm_tcgen05.cu): D = A B^T with A [batch][M][K] and
@@ -75,22 +86,6 @@ cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* par
 enum GemmMode : int {
   kRect = 0,      // every tile; write `out` (normal) and/or `outT` (transposed)
   kSymLower = 1,  // M == N, lower-triangle tiles only; `out` gets the tile and its mirror
-};
-
-// Fused row-scatter update for the final multiply-back of a Dion3 step: the
-// epilogue applies W[S] <- round_p(W[S] + neg_lr * D-value) from the fp32
-// accumulator instead of writing O.
-constexpr int kMaxUpdateBatch = 256;  // W pointers per launch
-struct GemmUpdate {
-  int enabled;
-  int tall;       // 1: D row r is selected row r (W[S[r]][c]); 0: D = O^T (W[S[c]][r])
-  int w_dtype;    // kBF16 or kF32
-  int w_cols;     // m: W row length and pitch
-  int w_rows;     // n: rows of W (bounds check of S)
-  int k;          // selected rows per matrix
-  const int32_t* idx;  // [batch][k] for the launch's matrices
-  float neg_lr;
-  void* W[kMaxUpdateBatch];
 };
 
 struct GemmDesc {
@@ -106,7 +101,6 @@ struct GemmDesc {
   // of a chain alternate the order, so each starts on the matrices the
   // previous one wrote last (still in L2).
   bool reverse = false;
-  const GemmUpdate* update = nullptr;  // fused W update (out / outT unused)
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

@@ -1,7 +1,6 @@
 // Memory-bound kernels of the Dion3 step: momentum accumulation with row
-// norms, l1 top-k selection, gather/normalise/transpose into fp16 and the sum
-// of squares used for normalisation.  (The row-scatter parameter update runs
-// in the epilogue of the final tensor-core GEMM.)
+// norms, l1 top-k selection, gather/normalise/transpose into fp16, the sum of
+// squares used for normalisation, and the row-scatter parameter update.
 //
 // Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of
 // the paper), third-level paragraph: rows are chosen by l1 norm, k = ceil(f n),
@@ -374,6 +373,70 @@ __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long lo
   }
 }
 
+// ---------------------------------------------------------------------------
+// a7: W[S_i] <- round_p(W[S_i] - lr O[i]).  One warp per selected row.
+// ---------------------------------------------------------------------------
+template <int PD, bool VEC>
+__global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ ScatterArgs a) {
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  if (gw >= total) return;
+  const int b = static_cast<int>(gw / a.k);
+  const int i = static_cast<int>(gw % a.k);
+  const int row = a.idx[static_cast<size_t>(b) * a.k + i];
+  if (row < 0 || row >= a.rows) {  // never expected: record and skip the access
+    if (lane == 0) atomicOr(a.status, kDevCheck);
+    return;
+  }
+  const __half* O = a.O + static_cast<long long>(b) * a.o_bstride + static_cast<size_t>(i) * a.ld_o;
+  const int cols = a.cols;
+  const float nlr = -a.lr;
+  if constexpr (PD == kBF16) {
+    __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(a.W[b]) + static_cast<size_t>(row) * cols;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < cols; c += kWarp * 8) {
+        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
+        const uint4 w = *reinterpret_cast<const uint4*>(W + c);
+        float wf[8];
+        bf16x8_to_f32(w, wf);
+        const __half2* oh = reinterpret_cast<const __half2*>(&o);
+        uint32_t outw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 of = __half22float2(oh[j]);
+          const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(nlr, of.x, wf[2 * j]), fmaf(nlr, of.y, wf[2 * j + 1]));
+          outw[j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
+        *reinterpret_cast<uint4*>(W + c) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      }
+    } else {
+      for (int c = lane; c < cols; c += kWarp)
+        W[c] = __float2bfloat16_rn(fmaf(nlr, __half2float(O[c]), __bfloat162float(W[c])));
+    }
+  } else {
+    float* W = reinterpret_cast<float*>(a.W[b]) + static_cast<size_t>(row) * cols;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < cols; c += kWarp * 8) {
+        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
+        const __half2* oh = reinterpret_cast<const __half2*>(&o);
+        float4 w0 = *reinterpret_cast<const float4*>(W + c);
+        float4 w1 = *reinterpret_cast<const float4*>(W + c + 4);
+        float2 o0 = __half22float2(oh[0]), o1 = __half22float2(oh[1]);
+        float2 o2 = __half22float2(oh[2]), o3 = __half22float2(oh[3]);
+        w0.x = fmaf(nlr, o0.x, w0.x); w0.y = fmaf(nlr, o0.y, w0.y);
+        w0.z = fmaf(nlr, o1.x, w0.z); w0.w = fmaf(nlr, o1.y, w0.w);
+        w1.x = fmaf(nlr, o2.x, w1.x); w1.y = fmaf(nlr, o2.y, w1.y);
+        w1.z = fmaf(nlr, o3.x, w1.z); w1.w = fmaf(nlr, o3.y, w1.w);
+        *reinterpret_cast<float4*>(W + c) = w0;
+        *reinterpret_cast<float4*>(W + c + 4) = w1;
+      }
+    } else {
+      for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, __half2float(O[c]), W[c]);
+    }
+  }
+}
+
 inline unsigned ceil_div(long long a, long long b) { return static_cast<unsigned>((a + b - 1) / b); }
 
 }  // namespace
@@ -414,6 +477,19 @@ cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
 cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts, int nparts,
                              cudaStream_t s) {
   sumsq_f16_kernel<<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  const dim3 grid(ceil_div(total, 8)), block(256);
+  if (a.param_dtype == kBF16) {
+    if (vec) scatter_kernel<kBF16, true><<<grid, block, 0, s>>>(a);
+    else scatter_kernel<kBF16, false><<<grid, block, 0, s>>>(a);
+  } else {
+    if (vec) scatter_kernel<kF32, true><<<grid, block, 0, s>>>(a);
+    else scatter_kernel<kF32, false><<<grid, block, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
