@@ -72,8 +72,9 @@ typedef enum { DION3_F32 = 0, DION3_BF16 = 1, DION3_F16 = 2 } dion3_dtype;
  *   restart_iter 0 for no restart, else 2..T: the 1-based iteration the
  *                restart comes before (the pages restart at iteration 3).
  *   a, b, c      the polynomial Z = aI + bR + cR^2.
- *   ns_dtype     arithmetic type of Gram-NS operands: DION3_F16 (fp32
- *                accumulation).  Other values return DION3_ERR_UNSUPPORTED.
+ *   ns_dtype     16-bit type of the Gram-NS operands and intermediates (fp32
+ *                accumulation): DION3_F16 (the pages' choice) or DION3_BF16.
+ *                Other values return DION3_ERR_UNSUPPORTED.
  */
 typedef struct {
   float f;
@@ -159,13 +160,13 @@ dion3_status dion3_gram_ns_workspace_size(int32_t k, int32_t m, int32_t batch,
                                           const dion3_hparams* hp, size_t* bytes);
 
 /*
- * Step (b) alone: Gram Newton-Schulz of `batch` fp16 k x m matrices.
- *   X  device fp16 [batch][k][m], read only.
- *   O  device fp16 [batch][k][m]: O = GramNS(X / (||X||_F + hp->eps)).
+ * Step (b) alone: Gram Newton-Schulz of `batch` k x m matrices.
+ *   X  device [batch][k][m] in hp->ns_dtype (fp16 or bf16), read only.
+ *   O  device [batch][k][m] in hp->ns_dtype: O = GramNS(X / (||X||_F + hp->eps)).
  * Only hp->eps, ns_steps, restart_iter, a, b, c and ns_dtype are used.
- * Operands are fp16 with fp32 accumulation; R, Z, Q and the products are
- * rounded to fp16 between steps (first-level paragraph: the method runs in
- * float16).
+ * Operands are fp16 (or bf16) with fp32 accumulation; R, Z, Q and the
+ * products are rounded to that type between steps (first-level paragraph: the
+ * method runs in float16).
  */
 dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const void* X,
                                    void* O, const dion3_hparams* hp, void* ws,

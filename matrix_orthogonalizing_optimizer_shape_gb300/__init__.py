@@ -279,7 +279,8 @@ def select_rows_noalloc(momentum: Sequence, grads: Optional[Sequence], k: int, i
 
 
 def gram_ns_batched(X, O, hp: HParams, ws, stream=None, ws_bytes: Optional[int] = None):
-    """Step (b): O = GramNS(X / (||X||_F + eps)) for fp16 X of shape [batch, k, m]."""
+    """Step (b): O = GramNS(X / (||X||_F + eps)) for X of shape [batch, k, m] in
+    hp.ns_dtype (fp16 or bf16)."""
     if X.dim() == 2:
         batch, (k, m) = 1, X.shape
     else:
@@ -320,7 +321,7 @@ def ns_workspace_size(variant: int, k: int, m: int, batch: int, hp: HParams) -> 
 
 
 def ns_batched(variant: int, X, O, hp: HParams, ws, stream=None, ws_bytes: Optional[int] = None):
-    """Newton-Schulz variant `variant` of fp16 X [batch, k, m] into O (see
+    """Newton-Schulz variant `variant` of X [batch, k, m] (hp.ns_dtype) into O (see
     dion3_ns_batched)."""
     if X.dim() == 2:
         batch, (k, m) = 1, X.shape

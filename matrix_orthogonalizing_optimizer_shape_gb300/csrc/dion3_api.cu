@@ -132,7 +132,8 @@ dion3_status check_hparams(const dion3_hparams* hp, bool need_step_fields) {
   if (!std::isfinite(hp->a) || !std::isfinite(hp->b) || !std::isfinite(hp->c))
     return fail(DION3_ERR_INVALID_ARG, "NS coefficients must be finite");
   if (!(hp->eps >= 0.0f) || !std::isfinite(hp->eps)) return fail(DION3_ERR_INVALID_ARG, "eps must be finite and >= 0");
-  if (hp->ns_dtype != DION3_F16) return fail(DION3_ERR_UNSUPPORTED, "ns_dtype: only DION3_F16 is implemented");
+  if (hp->ns_dtype != DION3_F16 && hp->ns_dtype != DION3_BF16)
+    return fail(DION3_ERR_UNSUPPORTED, "ns_dtype must be DION3_F16 or DION3_BF16");
   if (need_step_fields) {
     if (!(hp->f > 0.0f && hp->f <= 1.0f)) return fail(DION3_ERR_INVALID_ARG, "f must lie in (0, 1]");
     if (!std::isfinite(hp->mu)) return fail(DION3_ERR_INVALID_ARG, "mu must be finite");
@@ -238,9 +239,10 @@ cudaError_t traced_gather(const GatherArgs& g, bool vec, cudaStream_t s) {
   const double bytes = static_cast<double>(g.batch) * g.k * g.m * (per + 4.0);
   return traced("gather_normalize", 0.0, bytes, s, [&] { return launch_gather(g, vec, s); });
 }
-cudaError_t traced_sumsq(const __half* X, long long n, int batch, float* parts, int nparts, cudaStream_t s) {
+cudaError_t traced_sumsq(const __half* X, long long n, int batch, float* parts, int nparts, bool bf16,
+                         cudaStream_t s) {
   return traced("sumsq_f16", 0.0, 2.0 * n * batch, s,
-                [&] { return launch_sumsq_f16(X, n, batch, parts, nparts, s); });
+                [&] { return launch_sumsq_f16(X, n, batch, parts, nparts, bf16, s); });
 }
 cudaError_t traced_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const double pb = a.param_dtype == kBF16 ? 2.0 : 4.0;
@@ -302,6 +304,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   bool reverse = false;  // serpentine batch order across the chain
   auto launch = [&](const GemmDesc& g0) -> dion3_status {
     GemmDesc g = g0;
+    g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
     g.reverse = reverse;
     reverse = !reverse;
     const char* why = nullptr;
@@ -416,7 +419,9 @@ void gather_targets_std(const StdPlan& p, GatherArgs& g) {
 
 dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
                              cudaStream_t stream, bool dense) {
-  auto launch = [&](const GemmDesc& g) -> dion3_status {
+  auto launch = [&](const GemmDesc& g0) -> dion3_status {
+    GemmDesc g = g0;
+    g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
     const char* why = nullptr;
     if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
     const cudaError_t e = traced_gemm(g, st, stream);
@@ -664,12 +669,13 @@ dion3_status dion3_gram_ns_batched(int32_t k, int32_t m, int32_t batch, const vo
   constexpr int kParts = 64;
   float* parts = c.take<float>(static_cast<long long>(batch) * kParts);
   const long long n = static_cast<long long>(k) * m;
-  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, s);
+  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, hp->ns_dtype == DION3_BF16, s);
   if (e != cudaSuccess) return cuda_fail(e, "sumsq launch");
   GatherArgs g{};
   g.k = k; g.m = m; g.batch = batch; g.src_f32 = false;
   g.X = static_cast<const __half*>(X);
   g.fro2 = parts; g.fro2_parts = kParts; g.eps = hp->eps; g.decay = false;
+  g.bf16 = hp->ns_dtype == DION3_BF16;
   g.n = k; g.status = st;
   gather_targets(p, g);
   e = traced_gather(g, m % 4 == 0, s);
@@ -730,11 +736,12 @@ dion3_status dion3_ns_batched(int32_t variant, int32_t k, int32_t m, int32_t bat
   constexpr int kParts = 64;
   float* parts = c.take<float>(static_cast<long long>(batch) * kParts);
   const long long n = static_cast<long long>(k) * m;
-  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, s);
+  cudaError_t e = traced_sumsq(static_cast<const __half*>(X), n, batch, parts, kParts, hp->ns_dtype == DION3_BF16, s);
   if (e != cudaSuccess) return cuda_fail(e, "sumsq launch");
   g.k = k; g.m = m; g.batch = batch; g.src_f32 = false;
   g.X = static_cast<const __half*>(X);
   g.fro2 = parts; g.fro2_parts = kParts; g.eps = hp->eps; g.decay = false;
+  g.bf16 = hp->ns_dtype == DION3_BF16;
   g.n = k; g.status = st;
   e = traced_gather(g, m % 4 == 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
@@ -812,6 +819,7 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       for (int i = 0; i < nb; ++i) ga.M[i] = g.momentum[b0 + i];
       ga.idx = idx + static_cast<size_t>(b0) * gp.k;
       ga.fro2 = gp.fro2 + b0; ga.fro2_parts = 1; ga.eps = hp->eps; ga.mu = hp->mu; ga.decay = true;
+      ga.bf16 = hp->ns_dtype == DION3_BF16;
       ga.n = g.rows; ga.status = st;
       gather_targets(gp.ns, ga);
       ga.out_rows += ga.rows_bstride * b0;
@@ -830,6 +838,7 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       sa.O = gp.O + gp.o_bs * b0; sa.o_bstride = gp.o_bs; sa.ld_o = gp.ld_o;
       sa.lr = lr_eff;
       sa.status = st;
+      sa.o_bf16 = hp->ns_dtype == DION3_BF16;
       if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
   }

@@ -48,6 +48,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -268,11 +269,43 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
-// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28; M = 256 for the paired MMA (128 rows per CTA).
-__device__ __forceinline__ constexpr uint32_t idesc_f16_f32() {
-  return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B both fp16
+// (bits 7-9, 10-12 = 0) or both bf16 (= 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28; M = 256 for the paired MMA (128
+// rows per CTA).
+template <bool BF16>
+__device__ __forceinline__ constexpr uint32_t idesc_f32acc() {
+  return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>((2 * BM) >> 4) << 24);
+}
+
+// 16-bit element conversions of the two operand types (storage is 16-bit
+// words either way).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ float unpack1(uint16_t h) {
+  if constexpr (BF16) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  } else {
+    return __half2float(__ushort_as_half(h));
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  } else {
+    const __half2 t = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -333,6 +366,7 @@ __device__ __forceinline__ void prefetch_c(const GemmParams& p, int bidx, int r,
   }
 }
 
+template <bool BF16>
 __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
                                              const uint4 (&cv)[4], uint32_t (&hp)[16]) {
   float f[32];
@@ -343,11 +377,10 @@ __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int 
     if (c_vector_ok(p, c0)) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 u = cv[q];
-        const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+        const uint32_t w[4] = {cv[q].x, cv[q].y, cv[q].z, cv[q].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 x = __half22float2(h2[e]);
+          const float2 x = unpack2<BF16>(w[e]);
           f[8 * q + 2 * e] = fmaf(p.beta, x.x, f[8 * q + 2 * e]);
           f[8 * q + 2 * e + 1] = fmaf(p.beta, x.y, f[8 * q + 2 * e + 1]);
         }
@@ -355,7 +388,7 @@ __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int 
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (c0 + j < p.N) f[j] = fmaf(p.beta, __half2float(crow[j]), f[j]);
+        if (c0 + j < p.N) f[j] = fmaf(p.beta, unpack1<BF16>(__half_as_ushort(crow[j])), f[j]);
     }
   }
   if (p.gamma != 0.0f) {
@@ -368,10 +401,7 @@ __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int 
     for (int j = 0; j < 32; ++j) f[j] = 0.f;
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const __half2 t = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
-    hp[j] = *reinterpret_cast<const uint32_t*>(&t);
-  }
+  for (int j = 0; j < 16; ++j) hp[j] = pack2<BF16>(f[2 * j], f[2 * j + 1]);
 }
 
 __device__ __forceinline__ uint16_t half_bits(const uint32_t (&hp)[16], int j) {
@@ -411,6 +441,7 @@ __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx
   }
 }
 
+template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutT,
@@ -491,7 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_f16_f32();
+      constexpr uint32_t idesc = idesc_f32acc<BF16>();
       uint32_t kc = 0, tc = 0;
       bool ok = true;
       for (int u = cluster; u < p.total_units && ok; u += nclusters, ++tc) {
@@ -558,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
         uint32_t hp[16];
-        chunk_values(p, bidx, r, c0, v, cv, hp);
+        chunk_values<BF16>(p, bidx, r, c0, v, cv, hp);
         if (!tma_ok || (sym && row0 <= c0 + 31)) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp);
           continue;
@@ -629,7 +660,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 3-D tensor map over [batch][rows][cols] fp16 for the epilogue's bulk
 // stores: box 32 x 32 x 1 with the 64-byte swizzle of the staging buffers.
 bool make_store_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, int rows, int cols,
-                    int batch) {
+                    int batch, CUtensorMapDataType dt) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -637,7 +668,7 @@ bool make_store_map(CUtensorMap* map, const __half* ptr, long long bstride, int 
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, static_cast<cuuint64_t>(bstride) * 2u};
   cuuint32_t box[3] = {32u, 32u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
+  const CUresult r = fn(map, dt, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -654,7 +685,7 @@ bool storable(const __half* ptr, int ld, long long bstride, int rows, int batch)
 // 3-D tensor map over [batch][rows][cols] fp16 with row pitch `ld` elements,
 // box = 64 columns x box_rows rows x 1 matrix, 128-byte swizzle, zero fill.
 bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, int rows, int cols, int batch,
-              int box_rows) {
+              int box_rows, CUtensorMapDataType dt) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -662,7 +693,7 @@ bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, in
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, static_cast<cuuint64_t>(bstride) * 2u};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
+  const CUresult r = fn(map, dt, 3, const_cast<__half*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -677,7 +708,7 @@ int max_active_clusters(int dev) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Smem::kDyn;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<false>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
       int sms = 0;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -705,23 +736,26 @@ bool gemm_check(const GemmDesc& g, const char** why) {
   if (g.mode == kSymLower && (g.M != g.N || g.out == nullptr)) return fail("gemm: symmetric mode needs M == N and out");
   if (g.mode == kRect && g.out == nullptr && g.outT == nullptr) return fail("gemm: no output");
   if (g.M > (1 << 24) || g.N > (1 << 24)) return fail("gemm: dimension too large");
+  if (g.elem != kF16 && g.elem != kBF16) return fail("gemm: element type must be fp16 or bf16");
   return true;
 }
 
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
-  auto kern = gemm_tcgen05_kernel;
-  static std::once_flag once[64];
+  const bool bf16 = g.elem == kBF16;
+  auto kern = bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  static std::once_flag once[64][2];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
-  std::call_once(once[dev & 63], [&] {
+  std::call_once(once[dev & 63][bf16 ? 1 : 0], [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
   });
   if (attr_err != cudaSuccess) return attr_err;
 
   CUtensorMap ta, tb;
-  if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2, dt)) return cudaErrorInvalidValue;
 
   CUtensorMap to, tt;
   memset(&to, 0, sizeof to);
@@ -729,11 +763,11 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   int tma_out = 0, tma_outT = 0;
   if (storable(g.out, g.ld_out, g.out_bstride, g.M, g.batch) &&
       make_store_map(&to, g.out, g.out_bstride > 0 ? g.out_bstride : static_cast<long long>(g.ld_out) * g.M,
-                     g.ld_out, g.M, g.N, g.batch))
+                     g.ld_out, g.M, g.N, g.batch, dt))
     tma_out = 1;
   if (g.mode == kRect && storable(g.outT, g.ld_outT, g.outT_bstride, g.N, g.batch) &&
       make_store_map(&tt, g.outT, g.outT_bstride > 0 ? g.outT_bstride : static_cast<long long>(g.ld_outT) * g.N,
-                     g.ld_outT, g.N, g.M, g.batch))
+                     g.ld_outT, g.N, g.M, g.batch, dt))
     tma_outT = 1;
 
   GemmParams p{};

@@ -47,7 +47,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 struct GatherArgs {
   int n;                           // rows of each source matrix (bounds check of idx)
   int k, m, batch;                 // batch <= kMaxBatchPerLaunch when src_f32
-  bool src_f32;                    // true: rows of fp32 M picked by idx; false: fp16 X
+  bool src_f32;                    // true: rows of fp32 M picked by idx; false: 16-bit X
+  bool bf16;                       // 16-bit type of X and of the outputs: bf16 (else fp16)
   float* M[kMaxBatchPerLaunch];    // src_f32: momentum pointers
   const int32_t* idx;              // src_f32: [batch][k]
   const __half* X;                 // !src_f32: [batch][k][m] contiguous
@@ -64,7 +65,7 @@ cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s);
 
 // Sum of squares of fp16 X [batch][n] into parts [batch][parts].
 cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts,
-                             int nparts, cudaStream_t s);
+                             int nparts, bool bf16, cudaStream_t s);
 
 // a7: W[S_i] <- round(W[S_i] - lr O[i]) for the selected rows.
 struct ScatterArgs {
@@ -74,6 +75,7 @@ struct ScatterArgs {
   const int32_t* idx;              // [batch][k]
   const __half* O; long long o_bstride; int ld_o;   // [k][ld_o]
   float lr;
+  bool o_bf16;                     // O holds bf16 (else fp16)
   unsigned* status;                // device status word (kDevCheck on a bad index)
 };
 cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s);
@@ -101,6 +103,7 @@ struct GemmDesc {
   // of a chain alternate the order, so each starts on the matrices the
   // previous one wrote last (still in L2).
   bool reverse = false;
+  int elem = kF16;  // operand / output element type: kF16 or kBF16 (16-bit storage either way)
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

@@ -30,6 +30,23 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&f)[8]) {
   }
 }
 
+// 16-bit operand elements of the Gram-NS path: fp16, or bf16 when BF16.
+template <bool BF16>
+__device__ __forceinline__ float e16_to_f32(uint16_t h) {
+  if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  else return __half2float(__ushort_as_half(h));
+}
+template <bool BF16>
+__device__ __forceinline__ float2 e16x2_to_f32(uint32_t w) {
+  if constexpr (BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  else return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+template <bool BF16>
+__device__ __forceinline__ __half f32_to_e16(float f) {
+  if constexpr (BF16) return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(f)));
+  else return __float2half_rn(f);
+}
+
 __device__ __forceinline__ float load_grad(const void* g, size_t i, int gd) {
   if (gd == kBF16) {
     const uint16_t h = reinterpret_cast<const uint16_t*>(g)[i];
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int kGRows = 32, kGCols = 128;
 
-template <bool SRC_F32, bool VEC>
+template <bool SRC_F32, bool VEC, bool BF16>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherArgs a) {
   // Column-major staging: a pitch of 34 halves (17 words) spreads the 2-byte
   // writes of a warp over 8 banks (4-way conflicts; a 16-byte-aligned pitch of
@@ -288,17 +305,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
         const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * a.m;
         if (full) {
           const uint2 x = *reinterpret_cast<const uint2*>(src + c);
-          const __half2 p0 = *reinterpret_cast<const __half2*>(&x.x);
-          const __half2 p1 = *reinterpret_cast<const __half2*>(&x.y);
-          v[0] = __low2float(p0); v[1] = __high2float(p0);
-          v[2] = __low2float(p1); v[3] = __high2float(p1);
+          const float2 p0 = e16x2_to_f32<BF16>(x.x), p1 = e16x2_to_f32<BF16>(x.y);
+          v[0] = p0.x; v[1] = p0.y;
+          v[2] = p1.x; v[3] = p1.y;
         } else {
           for (int j = 0; j < 4; ++j)
-            if (c + j < a.m) v[j] = __half2float(src[c + j]);
+            if (c + j < a.m) v[j] = e16_to_f32<BF16>(__half_as_ushort(src[c + j]));
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) h[j] = __float2half_rn(v[j] * inv);
+      for (int j = 0; j < 4; ++j) h[j] = f32_to_e16<BF16>(v[j] * inv);
       __half* dst = a.out_rows + static_cast<long long>(b) * a.rows_bstride + static_cast<size_t>(i) * a.ld_rows + c;
       if (full && (a.ld_rows % 4 == 0)) {
         uint2 w;
@@ -337,6 +353,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 
 // Sum of squares of fp16 X: grid (nparts, batch); part p covers a contiguous
 // chunk of matrix b.
+template <bool BF16>
 __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long long n, float* parts, int nparts) {
   __shared__ float red[8];
   const int b = blockIdx.y, p = blockIdx.x;
@@ -349,17 +366,17 @@ __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long lo
   if (vec) {
     for (long long i = lo + threadIdx.x * 8LL; i < hi; i += 256LL * 8) {
       const uint4 u = *reinterpret_cast<const uint4*>(x + i);
-      const __half2* hp = reinterpret_cast<const __half2*>(&u);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(hp[j]);
+        const float2 f = e16x2_to_f32<BF16>(w[j]);
         s = fmaf(f.x, f.x, s);
         s = fmaf(f.y, f.y, s);
       }
     }
   } else {
     for (long long i = lo + threadIdx.x; i < hi; i += 256) {
-      const float f = __half2float(x[i]);
+      const float f = e16_to_f32<BF16>(__half_as_ushort(x[i]));
       s = fmaf(f, f, s);
     }
   }
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long lo
 // ---------------------------------------------------------------------------
 // a7: W[S_i] <- round_p(W[S_i] - lr O[i]).  One warp per selected row.
 // ---------------------------------------------------------------------------
-template <int PD, bool VEC>
+template <int PD, bool VEC, bool BF16>
 __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ ScatterArgs a) {
   const int lane = threadIdx.x % kWarp;
   const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
@@ -400,11 +417,11 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
         const uint4 w = *reinterpret_cast<const uint4*>(W + c);
         float wf[8];
         bf16x8_to_f32(w, wf);
-        const __half2* oh = reinterpret_cast<const __half2*>(&o);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
         uint32_t outw[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 of = __half22float2(oh[j]);
+          const float2 of = e16x2_to_f32<BF16>(ow[j]);
           const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(nlr, of.x, wf[2 * j]), fmaf(nlr, of.y, wf[2 * j + 1]));
           outw[j] = *reinterpret_cast<const uint32_t*>(&r);
         }
@@ -412,18 +429,17 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
       }
     } else {
       for (int c = lane; c < cols; c += kWarp)
-        W[c] = __float2bfloat16_rn(fmaf(nlr, __half2float(O[c]), __bfloat162float(W[c])));
+        W[c] = __float2bfloat16_rn(fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), __bfloat162float(W[c])));
     }
   } else {
     float* W = reinterpret_cast<float*>(a.W[b]) + static_cast<size_t>(row) * cols;
     if constexpr (VEC) {
       for (int c = lane * 8; c < cols; c += kWarp * 8) {
         const uint4 o = *reinterpret_cast<const uint4*>(O + c);
-        const __half2* oh = reinterpret_cast<const __half2*>(&o);
         float4 w0 = *reinterpret_cast<const float4*>(W + c);
         float4 w1 = *reinterpret_cast<const float4*>(W + c + 4);
-        float2 o0 = __half22float2(oh[0]), o1 = __half22float2(oh[1]);
-        float2 o2 = __half22float2(oh[2]), o3 = __half22float2(oh[3]);
+        const float2 o0 = e16x2_to_f32<BF16>(o.x), o1 = e16x2_to_f32<BF16>(o.y);
+        const float2 o2 = e16x2_to_f32<BF16>(o.z), o3 = e16x2_to_f32<BF16>(o.w);
         w0.x = fmaf(nlr, o0.x, w0.x); w0.y = fmaf(nlr, o0.y, w0.y);
         w0.z = fmaf(nlr, o1.x, w0.z); w0.w = fmaf(nlr, o1.y, w0.w);
         w1.x = fmaf(nlr, o2.x, w1.x); w1.y = fmaf(nlr, o2.y, w1.y);
@@ -432,7 +448,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
         *reinterpret_cast<float4*>(W + c + 4) = w1;
       }
     } else {
-      for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, __half2float(O[c]), W[c]);
+      for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), W[c]);
     }
   }
 }
@@ -464,19 +480,30 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
   const dim3 grid(ceil_div(a.m, kGCols), ceil_div(a.k, kGRows), a.batch), block(256);
-  if (a.src_f32) {
-    if (vec) gather_kernel<true, true><<<grid, block, 0, s>>>(a);
-    else gather_kernel<true, false><<<grid, block, 0, s>>>(a);
+  if (a.bf16) {
+    if (a.src_f32) {
+      if (vec) gather_kernel<true, true, true><<<grid, block, 0, s>>>(a);
+      else gather_kernel<true, false, true><<<grid, block, 0, s>>>(a);
+    } else {
+      if (vec) gather_kernel<false, true, true><<<grid, block, 0, s>>>(a);
+      else gather_kernel<false, false, true><<<grid, block, 0, s>>>(a);
+    }
   } else {
-    if (vec) gather_kernel<false, true><<<grid, block, 0, s>>>(a);
-    else gather_kernel<false, false><<<grid, block, 0, s>>>(a);
+    if (a.src_f32) {
+      if (vec) gather_kernel<true, true, false><<<grid, block, 0, s>>>(a);
+      else gather_kernel<true, false, false><<<grid, block, 0, s>>>(a);
+    } else {
+      if (vec) gather_kernel<false, true, false><<<grid, block, 0, s>>>(a);
+      else gather_kernel<false, false, false><<<grid, block, 0, s>>>(a);
+    }
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts, int nparts,
+cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts, int nparts, bool bf16,
                              cudaStream_t s) {
-  sumsq_f16_kernel<<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
+  if (bf16) sumsq_f16_kernel<true><<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
+  else sumsq_f16_kernel<false><<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
   return cudaGetLastError();
 }
 
@@ -484,11 +511,21 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.k;
   const dim3 grid(ceil_div(total, 8)), block(256);
   if (a.param_dtype == kBF16) {
-    if (vec) scatter_kernel<kBF16, true><<<grid, block, 0, s>>>(a);
-    else scatter_kernel<kBF16, false><<<grid, block, 0, s>>>(a);
+    if (a.o_bf16) {
+      if (vec) scatter_kernel<kBF16, true, true><<<grid, block, 0, s>>>(a);
+      else scatter_kernel<kBF16, false, true><<<grid, block, 0, s>>>(a);
+    } else {
+      if (vec) scatter_kernel<kBF16, true, false><<<grid, block, 0, s>>>(a);
+      else scatter_kernel<kBF16, false, false><<<grid, block, 0, s>>>(a);
+    }
   } else {
-    if (vec) scatter_kernel<kF32, true><<<grid, block, 0, s>>>(a);
-    else scatter_kernel<kF32, false><<<grid, block, 0, s>>>(a);
+    if (a.o_bf16) {
+      if (vec) scatter_kernel<kF32, true, true><<<grid, block, 0, s>>>(a);
+      else scatter_kernel<kF32, false, true><<<grid, block, 0, s>>>(a);
+    } else {
+      if (vec) scatter_kernel<kF32, true, false><<<grid, block, 0, s>>>(a);
+      else scatter_kernel<kF32, false, false><<<grid, block, 0, s>>>(a);
+    }
   }
   return cudaGetLastError();
 }

@@ -82,8 +82,10 @@ def test_invalid_hparams_are_rejected(lib):
         h = _hp(**kw)
         assert lib.dion3_gram_ns_workspace_size(16, 32, 1, ctypes.byref(h), ctypes.byref(out)) == d3.ERR_INVALID_ARG
         assert lib.dion3_last_error()
-    h = _hp(ns_dtype=d3.BF16)
+    h = _hp(ns_dtype=d3.F32)  # Gram NS runs on 16-bit operands only
     assert lib.dion3_gram_ns_workspace_size(16, 32, 1, ctypes.byref(h), ctypes.byref(out)) == d3.ERR_UNSUPPORTED
+    h = _hp(ns_dtype=d3.BF16)
+    assert lib.dion3_gram_ns_workspace_size(16, 32, 1, ctypes.byref(h), ctypes.byref(out)) == d3.OK
 
 
 def _fake_group(rows, cols, batch, base=0x10000, param_dtype=d3.BF16, grad_dtype=d3.BF16, stride=1 << 24):
