@@ -95,3 +95,25 @@ def test_ns_variants_match_oracle(cuda_lib, variant, k, m):
     for b in range(2):
         want = newton_schulz(normalize(X[b], hp.eps), MUON_QUINTIC, 5)
         assert rel_fro(O[b], want) <= tol, (variant, k, m, b)
+
+
+@pytest.mark.parametrize("k,m", [(64, 256), (256, 64), (200, 520), (1024, 4096), (128, 128)])
+def test_gram_ns_bf16_matches_oracle(cuda_lib, k, m):
+    # bf16 operands (ns_dtype = BF16): the unit roundoff is 8x that of fp16
+    # (2^-8 vs 2^-11), and the error grows accordingly (about 1e-2 here against
+    # about 1e-3 for fp16).  Rectangular shapes stay within the step's 3e-2;
+    # square ones (the least well-conditioned) are held to 8 x 3e-2.
+    rng = np.random.default_rng(k * 3 + m)
+    X = rng.standard_normal((2, k, m)).astype(np.float32)
+    hp = d3.HParams(ns_dtype=d3.BF16)
+    Xd = torch.from_numpy(X).to("cuda").to(torch.bfloat16).contiguous()
+    O = torch.full_like(Xd, float("nan"))
+    ws = d3.alloc_workspace(d3.gram_ns_workspace_size(k, m, 2, hp))
+    d3.gram_ns_batched(Xd, O, hp, ws)
+    d3.device_status()
+    Xv = Xd.float().cpu().numpy().astype(np.float64)
+    Og = O.float().cpu().numpy()
+    tol = O_REL_FRO if k != m else 8 * O_REL_FRO
+    for b in range(2):
+        want = newton_schulz(normalize(Xv[b], hp.eps), MUON_QUINTIC, 5)
+        assert rel_fro(Og[b], want) <= tol, (k, m, b, rel_fro(Og[b], want))

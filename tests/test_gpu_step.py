@@ -122,3 +122,17 @@ def test_step_degenerate_shapes(cuda_lib, n, m, f):
     G = workloads.gaussian((n, m), 0.01, seed=7, dtype="bf16")
     mat = Mat(W, M, "bf16", "bf16")
     _step_and_compare([[mat]], [[G]], d3.HParams(f=f, mu=0.9, lr=0.01))
+
+
+def test_step_bf16_ns(cuda_lib):
+    # The whole step with bf16 Gram NS: indices and momentum are unaffected
+    # (bit-exact), O (recovered from fp32 parameters) within 3e-2.
+    d = workloads.single(seed=3)
+    mat = Mat(d["W"], d["M"], "f32", "f32")
+    hp = d3.HParams(f=0.5, mu=d["mu"], lr=d["lr"], ns_dtype=d3.BF16)
+    _step_and_compare([[mat]], [[d["G"]]], hp, check_o=True)
+    g = workloads.gapped(seed=1, steps=2)
+    mat = Mat(g["W"], g["M"], "bf16", "bf16")
+    hp = d3.HParams(f=g["f"], mu=g["mu"], lr=g["lr"], ns_dtype=d3.BF16)
+    for t in range(2):
+        _step_and_compare([[mat]], [[g["grads"][t]]], hp)
