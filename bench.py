@@ -233,7 +233,8 @@ def run_ours(args, rank, world, device_index):
     device = torch.device("cuda", device_index)
     d3.load_library()
     groups, desc = workload_groups(args.workload, args.max_batch)
-    hp_kwargs = dict(mu=0.95, lr=0.02, eps=1e-7, ns_steps=5, restart_iter=3)
+    hp_kwargs = dict(mu=0.95, lr=0.02, eps=1e-7, ns_steps=5, restart_iter=3,
+                     ns_dtype=d3.BF16 if args.ns_dtype == "bf16" else d3.F16)
     hp = d3.HParams(f=args.f, **hp_kwargs)
     flops_rank = useful_flops_total(groups, args.f, hp_kwargs, d3)
 
@@ -373,11 +374,11 @@ def run_ours(args, rank, world, device_index):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic",
+        "dtype": args.ns_dtype, "data": "synthetic",
         "config": {"workload": f"{desc}, f={args.f}", "f": args.f,
                    "matrices": sum(g[2] for g in groups), "params_per_gpu": sum(g[0] * g[1] * g[2] for g in groups),
                    "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
-                   "ns": "Gram NS T=5 restart@3, fp16 operands, fp32 accumulate",
+                   "ns": f"Gram NS T=5 restart@3, {args.ns_dtype} operands, fp32 accumulate",
                    "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
@@ -574,6 +575,8 @@ def main():
     ap.add_argument("--sweep-full", action="store_true",
                     help="with --workload sweep: every (s, aspect, batch) of the sweep grid")
     ap.add_argument("--f", type=float, default=0.25)
+    ap.add_argument("--ns-dtype", choices=["f16", "bf16"], default="f16",
+                    help="16-bit type of the Gram-NS operands (the pages use fp16)")
     ap.add_argument("--max-batch", type=int, default=0,
                     help="cap the matrices per shape group (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
