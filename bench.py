@@ -244,12 +244,21 @@ def run_ours(args, rank, world, device_index):
     sel = [torch.empty((s["batch"], d3.num_selected(args.f, s["rows"])), dtype=torch.int32,
                        device=device) for s in state]
     stream = torch.cuda.current_stream(device)
+    # Lazy decay (--lazy-decay): per-row pending factors, one [batch, rows]
+    # buffer per group, starting at 1.
+    scales = [torch.ones((st_["batch"], st_["rows"]), dtype=torch.float32, device=device) for st_ in state]
+
+    def do_step(grps, scl, sel_out, wsp):
+        if args.lazy_decay:
+            d3.step_lazy(grps, hp, scl, wsp, sel_idx_out=sel_out, stream=stream)
+        else:
+            d3.step(grps, hp, wsp, sel_idx_out=sel_out, stream=stream)
 
     def barrier():
         rank_barrier(world)
 
     for _ in range(args.warmup):
-        d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
+        do_step(cgroups, scales, sel, ws)
     d3.device_status(stream)
 
     # Timed region: K steps, per-launch events through the library trace.
@@ -261,7 +270,7 @@ def run_ours(args, rank, world, device_index):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        d3.step(cgroups, hp, ws, sel_idx_out=sel, stream=stream)
+        do_step(cgroups, scales, sel, ws)
     ev1.record(stream)
     torch.cuda.synchronize(device)
     barrier()
@@ -315,7 +324,7 @@ def run_ours(args, rank, world, device_index):
                     evs.append(copy_stream.record_event())
             for (gi, lo, hi), ev, sg in zip(pieces, evs, sub_groups):
                 stream.wait_event(ev)
-                d3.step([sg], hp, ws_e2e, sel_idx_out=[sel[gi][lo:hi]], stream=stream)
+                do_step([sg], [scales[gi][lo:hi]], [sel[gi][lo:hi]], ws_e2e)
             for x, h in zip(sel, host_sel):
                 h.copy_(x, non_blocking=True)
 
@@ -379,6 +388,7 @@ def run_ours(args, rank, world, device_index):
                    "matrices": sum(g[2] for g in groups), "params_per_gpu": sum(g[0] * g[1] * g[2] for g in groups),
                    "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
                    "ns": f"Gram NS T=5 restart@3, {args.ns_dtype} operands, fp32 accumulate",
+                   "momentum_decay": "lazy (dion3_step_lazy)" if args.lazy_decay else "eager (dion3_step)",
                    "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
@@ -575,6 +585,8 @@ def main():
     ap.add_argument("--sweep-full", action="store_true",
                     help="with --workload sweep: every (s, aspect, batch) of the sweep grid")
     ap.add_argument("--f", type=float, default=0.25)
+    ap.add_argument("--lazy-decay", action="store_true",
+                    help="dion3_step_lazy: the selected rows' decay is carried to the next step")
     ap.add_argument("--ns-dtype", choices=["f16", "bf16"], default="f16",
                     help="16-bit type of the Gram-NS operands (the pages use fp16)")
     ap.add_argument("--max-batch", type=int, default=0,

@@ -294,6 +294,39 @@ dion3_status dion3_trace_enable(int32_t on);
 dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32_t* count);
 
 /*
+ * dion3_step with the momentum decay left pending (lazy error feedback): the
+ * selected rows' decay M[S] <- mu M[S] is not written back; instead
+ * row_scale[g][b][i] = mu marks it, and the next lazy step applies it while
+ * accumulating, M <- fp32(fp32(s M) + G), before resetting the factor to 1.
+ * The sequence of selections, parameters and (flushed) momenta is bit-identical
+ * to dion3_step's; a step writes k x m x 4 fewer bytes.
+ *   row_scale  host array [ngroups] of device fp32 buffers [batch][rows],
+ *              caller-owned optimizer state; set every entry to 1 before the
+ *              first lazy step.  Between lazy steps the momentum a caller sees
+ *              in M is the accumulated, not yet decayed one: the true momentum
+ *              of row i is fp32(row_scale[i] M[i]) (dion3_flush_row_scale
+ *              writes it back, e.g. before a checkpoint or a switch to
+ *              dion3_step).
+ * Third-level paragraph of the summary page: error feedback decays only the
+ * selected rows; deferring that multiplication to the next accumulation does
+ * not change it.
+ */
+dion3_status dion3_step_lazy(const dion3_group* groups, int32_t ngroups,
+                             const dion3_hparams* hp, float* const* row_scale, void* ws,
+                             size_t ws_bytes, int32_t* const* sel_idx_out,
+                             dion3_stream_t stream);
+
+/*
+ * Applies pending lazy decays of one shape group: M[b][i] <- fp32(s M[b][i])
+ * for every row whose factor s = row_scale[b][i] is not 1, then s <- 1.
+ *   momentum   host array [batch] of device fp32 rows x cols matrices.
+ *   row_scale  device fp32 [batch][rows].
+ */
+dion3_status dion3_flush_row_scale(int32_t rows, int32_t cols, int32_t batch,
+                                   float* const* momentum, float* row_scale,
+                                   dion3_stream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word written by
  * bounded device-side waits, and returns DION3_OK, DION3_ERR_TIMEOUT or
  * DION3_ERR_DEVICE_CHECK (or DION3_ERR_CUDA if synchronisation fails).

@@ -39,7 +39,7 @@ EXPORTED = (
     "dion3_gram_ns_workspace_size", "dion3_gram_ns_batched", "dion3_workspace_size",
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
     "dion3_trace_collect", "dion3_select_rows_noalloc", "dion3_ns_useful_flops",
-    "dion3_ns_workspace_size", "dion3_ns_batched",
+    "dion3_ns_workspace_size", "dion3_ns_batched", "dion3_step_lazy", "dion3_flush_row_scale",
 )
 
 
@@ -91,6 +91,9 @@ _SIGS = {
     "dion3_step": (ctypes.c_int, [ctypes.POINTER(_Group), _i32, ctypes.POINTER(_HParams), _vp, _sz,
                                   ctypes.POINTER(_vp), _vp]),
     "dion3_device_status": (ctypes.c_int, [_vp]),
+    "dion3_step_lazy": (ctypes.c_int, [ctypes.POINTER(_Group), _i32, ctypes.POINTER(_HParams),
+                                       ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp), _vp]),
+    "dion3_flush_row_scale": (ctypes.c_int, [_i32, _i32, _i32, ctypes.POINTER(_vp), _vp, _vp]),
     "dion3_gemm_f16": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32,
                                       _vp, _i32, ctypes.c_int64, _vp, _i32, ctypes.c_int64,
                                       _vp, _i32, ctypes.c_int64, _vp, _i32, ctypes.c_int64,
@@ -374,6 +377,30 @@ def trace_collect() -> dict:
                                 "useful_flops": float(e.useful_flops),
                                 "algo_bytes": float(e.algo_bytes)}
     return out
+
+
+def step_lazy(groups: Sequence[Group], hp: HParams, row_scale: Sequence, ws,
+              sel_idx_out: Optional[Sequence] = None, stream=None, ws_bytes: Optional[int] = None):
+    """dion3_step with the selected rows' decay left pending in row_scale (one
+    fp32 [batch, rows] tensor per group, all ones before the first call); see
+    dion3_step_lazy."""
+    cg = (_Group * len(groups))(*[g.c_struct() for g in groups])
+    hs = hp.c_struct()
+    rs = (ctypes.c_void_p * len(groups))(*[_ptr(t) for t in row_scale])
+    sel = None
+    if sel_idx_out is not None:
+        sel = (ctypes.c_void_p * len(groups))(*[_ptr(t) for t in sel_idx_out])
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(load_library().dion3_step_lazy(cg, len(groups), ctypes.byref(hs), rs, _ptr(ws), nbytes, sel,
+                                          _stream(stream)))
+
+
+def flush_row_scale(momentum: Sequence, row_scale, stream=None):
+    """Apply pending lazy decays of one group in place (dion3_flush_row_scale)."""
+    n = len(momentum)
+    rows, cols = momentum[0].shape
+    M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momentum])
+    _check(load_library().dion3_flush_row_scale(rows, cols, n, M, _ptr(row_scale), _stream(stream)))
 
 
 def device_status(stream=None):

@@ -769,8 +769,15 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups, co
   return ok();
 }
 
-dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp, void* ws,
-                        size_t ws_bytes, int32_t* const* sel_idx_out, dion3_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// The step of dion3_step; with row_scale (one [batch][rows] fp32 buffer per
+// group) the decay of the selected momentum rows is left pending in row_scale
+// instead of being written back (dion3_step_lazy).
+dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp, void* ws,
+                       size_t ws_bytes, int32_t* const* sel_idx_out, float* const* row_scale,
+                       dion3_stream_t stream) {
   size_t need = 0;
   dion3_status rc = dion3_workspace_size(groups, ngroups, hp, &need);
   if (rc != DION3_OK) return rc;
@@ -780,6 +787,10 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
     for (int i = 0; i < ngroups; ++i)
       if (sel_idx_out[i] != nullptr && (reinterpret_cast<uintptr_t>(sel_idx_out[i]) & 3u))
         return fail(DION3_ERR_INVALID_ARG, "sel_idx_out[%d] must be 4-byte aligned", i);
+  if (row_scale != nullptr)
+    for (int i = 0; i < ngroups; ++i)
+      if (row_scale[i] == nullptr || (reinterpret_cast<uintptr_t>(row_scale[i]) & 3u))
+        return fail(DION3_ERR_INVALID_ARG, "row_scale[%d] must be a 4-byte aligned device pointer", i);
   if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
   if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
   unsigned* st = device_status_ptr();
@@ -806,6 +817,7 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       }
       a.l1 = gp.l1 + static_cast<size_t>(b0) * g.rows;
       a.sq = gp.sq + static_cast<size_t>(b0) * g.rows;
+      if (row_scale != nullptr) a.scale = row_scale[gi] + static_cast<size_t>(b0) * g.rows;
       if ((e = traced_accum(a, vec, s)) != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
     }
     TopkArgs t{};
@@ -818,7 +830,9 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       ga.k = gp.k; ga.m = g.cols; ga.batch = nb; ga.src_f32 = true;
       for (int i = 0; i < nb; ++i) ga.M[i] = g.momentum[b0 + i];
       ga.idx = idx + static_cast<size_t>(b0) * gp.k;
-      ga.fro2 = gp.fro2 + b0; ga.fro2_parts = 1; ga.eps = hp->eps; ga.mu = hp->mu; ga.decay = true;
+      ga.fro2 = gp.fro2 + b0; ga.fro2_parts = 1; ga.eps = hp->eps; ga.mu = hp->mu;
+      ga.decay = row_scale == nullptr;
+      if (row_scale != nullptr) ga.scale_out = row_scale[gi] + static_cast<size_t>(b0) * g.rows;
       ga.bf16 = hp->ns_dtype == DION3_BF16;
       ga.n = g.rows; ga.status = st;
       gather_targets(gp.ns, ga);
@@ -841,6 +855,43 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_
       sa.o_bf16 = hp->ns_dtype == DION3_BF16;
       if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
+  }
+  return ok();
+}
+}  // namespace
+
+extern "C" {
+
+dion3_status dion3_step(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp, void* ws,
+                        size_t ws_bytes, int32_t* const* sel_idx_out, dion3_stream_t stream) {
+  return step_impl(groups, ngroups, hp, ws, ws_bytes, sel_idx_out, nullptr, stream);
+}
+
+dion3_status dion3_step_lazy(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp,
+                             float* const* row_scale, void* ws, size_t ws_bytes, int32_t* const* sel_idx_out,
+                             dion3_stream_t stream) {
+  if (row_scale == nullptr) return fail(DION3_ERR_INVALID_ARG, "row_scale must not be NULL");
+  return step_impl(groups, ngroups, hp, ws, ws_bytes, sel_idx_out, row_scale, stream);
+}
+
+dion3_status dion3_flush_row_scale(int32_t rows, int32_t cols, int32_t batch, float* const* momentum,
+                                   float* row_scale, dion3_stream_t stream) {
+  if (rows < 1 || cols < 1 || batch < 1) return fail(DION3_ERR_INVALID_ARG, "need rows, cols, batch >= 1");
+  if (momentum == nullptr || row_scale == nullptr || (reinterpret_cast<uintptr_t>(row_scale) & 3u))
+    return fail(DION3_ERR_INVALID_ARG, "momentum and a 4-byte aligned row_scale are required");
+  for (int b = 0; b < batch; ++b)
+    if (momentum[b] == nullptr || (reinterpret_cast<uintptr_t>(momentum[b]) & 3u))
+      return fail(DION3_ERR_INVALID_ARG, "momentum[%d] NULL or misaligned", b);
+  if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int b0 = 0; b0 < batch; b0 += kMaxBatchPerLaunch) {
+    const int nb = std::min(kMaxBatchPerLaunch, batch - b0);
+    FlushArgs a{};
+    a.rows = rows; a.cols = cols; a.batch = nb;
+    for (int i = 0; i < nb; ++i) a.M[i] = momentum[b0 + i];
+    a.scale = row_scale + static_cast<size_t>(b0) * rows;
+    const cudaError_t e = launch_flush_scale(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   }
   return ok();
 }

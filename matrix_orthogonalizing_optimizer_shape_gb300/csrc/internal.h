@@ -28,6 +28,9 @@ struct AccumArgs {
   const void* G[kMaxBatchPerLaunch]; // all null: norms only
   float* l1;                         // [batch][rows]
   float* sq;                         // [batch][rows]
+  // Lazy decay: pending per-row factor s ([batch][rows]); the accumulation
+  // becomes M <- fp32(fp32(s M) + G) and s is reset to 1.  Null: s = 1.
+  float* scale = nullptr;
 };
 cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s);
 
@@ -57,11 +60,21 @@ struct GatherArgs {
   float eps;
   float mu;                        // decay applied to the source rows (src_f32)
   bool decay;
+  float* scale_out = nullptr;      // lazy decay: scale_out[b][row] = mu for the selected rows
   unsigned* status;                // device status word (kDevCheck on a bad index)
   __half* out_rows; long long rows_bstride; int ld_rows;   // [k][ld_rows]
   __half* out_cols; long long cols_bstride; int ld_cols;   // [m][ld_cols]
 };
 cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s);
+
+// Lazy decay made explicit: M[b][r] <- fp32(scale[b][r] M[b][r]) where the
+// factor is not 1, then the factor is reset to 1.
+struct FlushArgs {
+  int rows, cols, batch;             // batch <= kMaxBatchPerLaunch
+  float* M[kMaxBatchPerLaunch];
+  float* scale;                      // [batch][rows]
+};
+cudaError_t launch_flush_scale(const FlushArgs& a, cudaStream_t s);
 
 // Sum of squares of fp16 X [batch][n] into parts [batch][parts].
 cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts,

@@ -72,6 +72,9 @@ __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constan
   const int cols = a.cols;
   float* __restrict__ Mrow = a.M[b] + static_cast<size_t>(r) * cols;
   float l1 = 0.f, sq = 0.f;
+  // Pending lazy decay of this row (warp-uniform); only with a gradient.
+  const float rs = (GD >= 0 && a.scale != nullptr) ? a.scale[gw] : 1.0f;
+  const bool scaled = rs != 1.0f;
 
   if constexpr (VEC) {
     constexpr int U = 2;  // iterations of loads kept in flight (2 measured fastest: more resident warps)
@@ -104,6 +107,10 @@ __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constan
         const int c = c0 + u * step;
         if (c < cols) {
           if constexpr (GD >= 0) {
+            if (scaled) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) m[u][j] = __fmul_rn(rs, m[u][j]);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) m[u][j] = __fadd_rn(m[u][j], g[u][j]);
             *reinterpret_cast<float4*>(Mrow + c) = make_float4(m[u][0], m[u][1], m[u][2], m[u][3]);
@@ -121,6 +128,7 @@ __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constan
     for (int c = lane; c < cols; c += kWarp) {
       float m = Mrow[c];
       if constexpr (GD >= 0) {
+        if (scaled) m = __fmul_rn(rs, m);
         m = __fadd_rn(m, load_grad(a.G[b], static_cast<size_t>(r) * cols + c, GD));
         Mrow[c] = m;
       }
@@ -133,6 +141,7 @@ __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constan
   if (lane == 0) {
     a.l1[gw] = l1;
     a.sq[gw] = sq;
+    if (GD >= 0 && a.scale != nullptr && scaled) a.scale[gw] = 1.0f;
   }
 }
 
@@ -264,6 +273,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
   const int c0 = blockIdx.x * kGCols;
   const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
 
+  if constexpr (SRC_F32) {
+    // Lazy decay: record the pending factor of each selected row once (by the
+    // CTAs of the first column tile) instead of writing mu M back.
+    if (a.scale_out != nullptr && blockIdx.x == 0 && threadIdx.x < kGRows && i0 + threadIdx.x < a.k) {
+      const int row = a.idx[static_cast<size_t>(b) * a.k + i0 + threadIdx.x];
+      if (row >= 0 && row < a.n) a.scale_out[static_cast<size_t>(b) * a.n + row] = a.mu;
+    }
+  }
   float f2 = 0.f;
   for (int p = 0; p < a.fro2_parts; ++p) f2 += a.fro2[static_cast<size_t>(b) * a.fro2_parts + p];
   const float inv = 1.0f / (sqrtf(f2) + a.eps);
@@ -453,6 +470,21 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
   }
 }
 
+// M[b][r] <- fp32(s M[b][r]) for rows whose pending factor s is not 1; s <- 1.
+// One warp per row; rows with s = 1 cost one load.
+__global__ void __launch_bounds__(256) flush_scale_kernel(const __grid_constant__ FlushArgs a) {
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  if (gw >= static_cast<long long>(a.batch) * a.rows) return;
+  const float s = a.scale[gw];
+  if (s == 1.0f) return;
+  const int b = static_cast<int>(gw / a.rows), r = static_cast<int>(gw % a.rows);
+  float* row = a.M[b] + static_cast<size_t>(r) * a.cols;
+  for (int c = lane; c < a.cols; c += kWarp) row[c] = __fmul_rn(s, row[c]);
+  __syncwarp();
+  if (lane == 0) a.scale[gw] = 1.0f;
+}
+
 inline unsigned ceil_div(long long a, long long b) { return static_cast<unsigned>((a + b - 1) / b); }
 
 }  // namespace
@@ -470,6 +502,12 @@ cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s) {
     else if (a.grad_dtype == kBF16) accum_rownorm_kernel<false, kBF16><<<grid, block, 0, s>>>(a);
     else accum_rownorm_kernel<false, kF32><<<grid, block, 0, s>>>(a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flush_scale(const FlushArgs& a, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.batch) * a.rows;
+  flush_scale_kernel<<<ceil_div(total, 8), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
