@@ -35,7 +35,9 @@
 //                  accumulators in both CTAs with multicast commits;
 //   warps 2..9     epilogue (both CTAs): two warps per TMEM lane quadrant
 //                  (warp % 4), each taking half of the 256 columns, 32 at a
-//                  time: tcgen05.ld, alpha/beta/gamma, then the 32 x 32 box
+//                  time (C, when given, is loaded for the whole tile before
+//                  the accumulator is ready): tcgen05.ld, alpha/beta/gamma,
+//                  then the 32 x 32 box
 //                  (and its transpose) staged in swizzled shared memory and
 //                  written with bulk tensor stores (chunks on the diagonal of
 //                  a symmetric result are written element by element); then
@@ -352,8 +354,9 @@ struct Smem {
 // row r; v[j] is column c0 + j of the fp32 accumulator.  hp receives
 // alpha D + beta C + gamma I as packed fp16 pairs (rows r >= M give zeros and
 // read nothing).
-// The C operand of a chunk in 16-byte pieces, loaded before the TMEM read so
-// the two latencies overlap (only when the chunk is full and C's pitch allows
+// The C operand of a chunk in 16-byte pieces.  A warp loads the C values of
+// all its chunks of a tile before it waits for the accumulator, so the load
+// latency overlaps the MMAs (only when the chunk is full and C's pitch allows
 // vector loads; otherwise chunk_values reads C element-wise).
 __device__ __forceinline__ bool c_vector_ok(const GemmParams& p, int c0) {
   return p.C != nullptr && (c0 + 32 <= p.N) && (p.ldc % 8 == 0);
@@ -554,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps 2 .. 2 + kEpiWarps - 1 ----------------
     const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
     const int col_lo = ((warp - 2) / 4) * (BN * 4 / kEpiWarps);  // this warp's columns of the tile
-    const int col_hi = col_lo + BN * 4 / kEpiWarps;
+    constexpr int kChunks = BN * 4 / kEpiWarps / 32;  // 32-column chunks per warp and tile
     const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * Smem::kWarpStagingBytes;
     const bool sym = p.mode == kSymLower;
     // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
@@ -571,25 +574,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       unit_coords(p, u % p.units_per_mat, P, bc);
       const int bi = 2 * P + static_cast<int>(rank);
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+      const int row0 = bi * BM + quad * 32;
+      const int r = row0 + lane;
+      // C of every chunk this warp will write (registers; unused entries stay
+      // unread, the conditions match the chunk loop below).
+      uint4 cvs[kChunks][4];
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int c0 = bc * BN + col_lo + 32 * i;
+        if (c0 < p.N && !(sym && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
+      }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
       if (!ok) break;
       tc_fence_after();
-      const int row0 = bi * BM + quad * 32;
-      const int r = row0 + lane;
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
-      for (int cc = col_lo; cc < col_hi; cc += 32) {
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int cc = col_lo + 32 * i;
         const int c0 = bc * BN + cc;
         // Warp-uniform classification of the chunk.
         if (c0 >= p.N) break;
         if (sym && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
         if (row0 >= p.M) continue;            // rows out of range
-        uint4 cv[4];
-        prefetch_c(p, bidx, r, c0, cv);
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
         uint32_t hp[16];
-        chunk_values<BF16>(p, bidx, r, c0, v, cv, hp);
+        chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
         if (!tma_ok || (sym && row0 <= c0 + 31)) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp);
           continue;
