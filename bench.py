@@ -19,6 +19,9 @@ Printed (rank 0, one JSON line):
                peak in MEASURED_PEAKS.json.
   cpu_baseline the float64 CPU oracle timed on a bounded sample (one matrix of
                each shape group) and scaled to the full set.
+  per_model    (default workload only) step ms and useful TFLOP/s with their
+               fraction of the measured bf16 peak for each model at each f:
+               7B at f = 1/4 (the headline) and 1/8, 1B at f = 1, 1/2, 1/4.
 
 --impl reference times the CPU oracle (the only reference this method has:
 there is no reference implementation to install) on the same workload and
@@ -225,6 +228,63 @@ def cpu_baseline(state, groups, f, hp, flops_total):
                       + "; ".join(parts) + ")"}
 
 
+#: The (model, f) points of the per-model table printed with the default
+#: workload (the 7B f = 1/4 point is the headline measurement itself).
+PER_MODEL_POINTS = (("7b", 0.125), ("1b", 1.0), ("1b", 0.5), ("1b", 0.25))
+
+
+def time_steps(state, hp, d3, device, stream, world, steps, warmup, lazy):
+    """Device ms per dion3_step (or dion3_step_lazy) over every group of
+    `state`, CUDA events on `stream` after `warmup` untimed steps; max over
+    ranks."""
+    import torch
+    cg = [st_["group"] for st_ in state]
+    ws = d3.alloc_workspace(d3.workspace_size(cg, hp), device=device)
+    sel = [torch.empty((st_["batch"], d3.num_selected(hp.f, st_["rows"])), dtype=torch.int32, device=device)
+           for st_ in state]
+    scales = [torch.ones((st_["batch"], st_["rows"]), dtype=torch.float32, device=device) for st_ in state]
+
+    def one():
+        if lazy:
+            d3.step_lazy(cg, hp, scales, ws, sel_idx_out=sel, stream=stream)
+        else:
+            d3.step(cg, hp, ws, sel_idx_out=sel, stream=stream)
+
+    for _ in range(warmup):
+        one()
+    rank_barrier(world)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    rank_barrier(world)
+    d3.device_status(stream)
+    ms = e0.elapsed_time(e1) / steps
+    del ws, sel, scales
+    return max_over_ranks(ms, world, device)
+
+
+def per_model_table(args, world, device, stream, d3, hp_kwargs, main_state, head_row, peak):
+    """ms and useful TFLOP/s of the step for each (model, f) point: the 7B
+    set (already resident) at the other f, then the 1B set, built for it."""
+    rows = [head_row]
+    states = {"7b": main_state}
+    for model, f in PER_MODEL_POINTS:
+        groups, _ = workload_groups(model)
+        if model not in states:
+            states[model] = build_state(groups, device, 11, d3)
+        hp = d3.HParams(f=f, **hp_kwargs)
+        flops = useful_flops_total(groups, f, hp_kwargs, d3)
+        ms = time_steps(states[model], hp, d3, device, stream, world, args.per_model_steps, 3, args.lazy_decay)
+        tflops = job_tflops(flops, world, ms)
+        rows.append({"model": model.upper(), "f": f, "ms_per_step": ms, "useful_tflops": tflops,
+                     "frac_of_fp16_peak": tflops / world / peak})
+    return rows
+
+
 def run_ours(args, rank, world, device_index):
     import torch
     import matrix_orthogonalizing_optimizer_shape_gb300 as d3
@@ -346,6 +406,15 @@ def run_ours(args, rank, world, device_index):
                "h2d_gbs": h2d / (ems * 1e-3) / 1e9}
         del host_g, ws_e2e
 
+    per_model = None
+    if args.workload == "7b" and args.f == 0.25 and args.max_batch == 0 and not args.no_per_model:
+        peaks0, _ = load_peaks()
+        peak0 = peaks0.get("bf16_tflops_sustained") or peaks0["bf16_tflops"]
+        head = {"model": "7B", "f": args.f, "ms_per_step": ms_max,
+                "useful_tflops": job_tflops(flops_rank, world, ms_max),
+                "frac_of_fp16_peak": job_tflops(flops_rank, world, ms_max) / world / peak0}
+        per_model = per_model_table(args, world, device, stream, d3, hp_kwargs, state, head, peak0)
+
     if rank != 0:
         return None
 
@@ -398,6 +467,8 @@ def run_ours(args, rank, world, device_index):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if per_model is not None:
+        line["per_model"] = per_model
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(state, groups, args.f, hp, flops_rank)
     return line
@@ -595,6 +666,10 @@ def main():
     ap.add_argument("--e2e-chunk", type=int, default=16,
                     help="matrices per pipelined sub-batch in the end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-model", action="store_true",
+                    help="skip the per-model table (7B at f = 1/8, 1B at f = 1, 1/2, 1/4)")
+    ap.add_argument("--per-model-steps", type=int, default=10,
+                    help="timed steps per point of the per-model table")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
