@@ -206,6 +206,21 @@ dion3_status dion3_ns_batched(int32_t variant, int32_t k, int32_t m, int32_t bat
 typedef enum { DION3_GEMM_RECT = 0, DION3_GEMM_SYM_LOWER = 1 } dion3_gemm_mode;
 
 /*
+ * Flags or-ed into the mode of dion3_gemm_f16 for half-stored symmetric
+ * matrices.  A half-stored symmetric s x s matrix holds valid values only in
+ * the 256 x 256 blocks below the block diagonal and in the full diagonal
+ * 256 x 256 blocks (both triangles, mirrored); the rest is never written nor
+ * read.  This is the layout of the s x s matrices inside the Gram
+ * Newton-Schulz path (dion3_gram_ns_batched / dion3_step).
+ *   DION3_GEMM_OUT_HALF: with DION3_GEMM_SYM_LOWER, write D half-stored (the
+ *                        mirror is written on the diagonal blocks only).
+ *   DION3_GEMM_A_HALF:   A is half-stored (needs M == K); the part of A above
+ *                        the diagonal blocks is read from its transpose.
+ *   DION3_GEMM_B_HALF:   B is half-stored (needs N == K), likewise.
+ */
+enum { DION3_GEMM_OUT_HALF = 0x10, DION3_GEMM_A_HALF = 0x20, DION3_GEMM_B_HALF = 0x40 };
+
+/*
  * The tensor-core GEMM behind step (b), callable on its own.  Second-level
  * paragraph of the summary page: a symmetric product needs only its lower
  * triangle, which is then copied to the upper one.  Computes
@@ -222,8 +237,11 @@ typedef enum { DION3_GEMM_RECT = 0, DION3_GEMM_SYM_LOWER = 1 } dion3_gemm_mode;
  *                         symmetric (DT must be NULL).  Correct whenever
  *                         A B^T is symmetric: A == B, or A and B commuting
  *                         symmetric matrices (then B^T = B).
+ *   The mode may carry the DION3_GEMM_*_HALF flags above.
  * Rules: A and B 16-byte aligned; lda, ldb >= K and multiples of 8; their batch
  * strides multiples of 8.  D, DT and C may have any pitch >= their row length.
+ * An unknown mode or flag, or a flag whose shape rule does not hold, returns
+ * DION3_ERR_INVALID_ARG with nothing launched.
  */
 dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t batch,
                             const void* A, int32_t lda, int64_t a_bstride,

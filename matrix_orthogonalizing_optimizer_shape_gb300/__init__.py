@@ -337,6 +337,10 @@ def ns_batched(variant: int, X, O, hp: HParams, ws, stream=None, ws_bytes: Optio
 
 
 GEMM_RECT, GEMM_SYM_LOWER = 0, 1
+#: Mode flags for half-stored symmetric matrices (see dion3_gemm_f16): only the
+#: 256 x 256 blocks below the block diagonal and the full diagonal blocks hold
+#: valid values.
+GEMM_OUT_HALF, GEMM_A_HALF, GEMM_B_HALF = 0x10, 0x20, 0x40
 
 
 def gemm_f16(A, B, D=None, DT=None, C=None, *, mode: int = GEMM_RECT, alpha: float = 1.0,

@@ -294,8 +294,14 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     g.B = B; g.b_bstride = from_y ? p.y_bs : p.s_bs; g.ldb = from_y ? p.Lp : p.sp;
     g.M = p.s; g.N = p.s; g.K = K; g.batch = p.batch;
     // dense: every tile of the product (the comparison path without the
-    // symmetric savings); otherwise lower-triangle tiles, mirrored.
+    // symmetric savings); otherwise lower-triangle tiles.  Every s x s matrix
+    // of the chain is then half-stored (the 256 x 256 blocks below the block
+    // diagonal and the full diagonal blocks): written without the mirror
+    // outside the diagonal blocks, and read back with the K ranges above the
+    // diagonal taken from the transpose.
     g.mode = dense ? kRect : kSymLower;
+    g.out_half = !dense;
+    g.a_half = g.b_half = !dense && !from_y;
     g.alpha = alpha; g.beta = beta; g.gamma = gamma;
     g.C = C; g.c_bstride = p.s_bs; g.ldc = p.sp;
     g.out = D; g.out_bstride = p.s_bs; g.ld_out = p.sp;
@@ -335,6 +341,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
       g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
       g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
       g.mode = kRect; g.alpha = 1.f;
+      g.b_half = !dense;
       g.out = p.Yt[ycur ^ 1]; g.out_bstride = p.yt_bs; g.ld_out = p.sp;
       g.outT = p.Y; g.outT_bstride = p.y_bs; g.ld_outT = p.Lp;
       if ((rc = launch(g)) != DION3_OK) return rc;
@@ -365,6 +372,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
   g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
   g.mode = kRect; g.alpha = 1.f;
+  g.b_half = !dense;
   if (p.wide) {
     g.outT = out.O; g.outT_bstride = out.o_bs; g.ld_outT = out.ld_o;
   } else {
@@ -901,7 +909,11 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
                             const void* C, int32_t ldc, int64_t c_bstride, void* D, int32_t ldd,
                             int64_t d_bstride, void* DT, int32_t lddt, int64_t dt_bstride, float alpha,
                             float beta, float gamma, dion3_stream_t stream) {
+  const int32_t flags = mode & ~0xF;
+  mode &= 0xF;
   if (mode != DION3_GEMM_RECT && mode != DION3_GEMM_SYM_LOWER) return fail(DION3_ERR_INVALID_ARG, "bad GEMM mode");
+  if ((flags & ~(DION3_GEMM_OUT_HALF | DION3_GEMM_A_HALF | DION3_GEMM_B_HALF)) != 0)
+    return fail(DION3_ERR_INVALID_ARG, "unknown GEMM mode flag");
   if (M < 1 || N < 1 || K < 1 || batch < 1 || batch > 65535)
     return fail(DION3_ERR_INVALID_ARG, "need M, N, K >= 1 and 1 <= batch <= 65535");
   if (mode == DION3_GEMM_SYM_LOWER && (M != N || D == nullptr || DT != nullptr))
@@ -923,6 +935,9 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
   g.C = static_cast<const __half*>(C); g.c_bstride = c_bstride; g.ldc = ldc;
   g.out = static_cast<__half*>(D); g.out_bstride = d_bstride; g.ld_out = ldd;
   g.outT = static_cast<__half*>(DT); g.outT_bstride = dt_bstride; g.ld_outT = lddt;
+  g.out_half = (flags & DION3_GEMM_OUT_HALF) != 0;
+  g.a_half = (flags & DION3_GEMM_A_HALF) != 0;
+  g.b_half = (flags & DION3_GEMM_B_HALF) != 0;
   const char* why = nullptr;
   if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "%s", why);
   if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");

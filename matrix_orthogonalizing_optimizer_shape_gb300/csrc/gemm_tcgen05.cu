@@ -9,6 +9,19 @@
 // exactly symmetric.  In kRect mode every tile is computed and written in the
 // normal and/or the transposed orientation.
 //
+// Half-stored symmetric matrices.  A symmetric s x s result may instead be
+// written as its lower triangle at 256 x 256 block granularity: the blocks
+// below the diagonal and the full diagonal blocks (mirrored inside), nothing
+// above (out_half).  Such a matrix is read back as an operand (a_half /
+// b_half): a K range of 64 that lies within or left of the operand rows'
+// diagonal block is loaded K-major from the rows themselves; a K range right
+// of it, where S[m][k] is above the diagonal, is loaded from S[k][m] (below
+// it) as an MN-major tile: two 64 x 64 boxes, read by the MMA with the
+// MN-major bit of the instruction descriptor set.  Both CTAs of a pair have
+// the same 256-row super-row, so they always agree on the orientation.  This
+// skips the mirror writes outside the diagonal blocks and never touches the
+// upper triangle.
+//
 // Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of the
 // paper).  First-level paragraph: Newton-Schulz iterates on the small
 // symmetric Gram matrix X X^T and multiplies back by X at the end.  Second-level
@@ -26,13 +39,15 @@
 // 128 r .. 128 r + 127 of A and rows 128 r .. 128 r + 127 of the B panel in its
 // own shared memory, and receives rows 128 r .. of the result in its own TMEM.
 // A ring slot therefore holds 32 KB per CTA (its A tile and its half of B), so
-// the 192 KB ring is 6 slots deep.  6 warps per CTA:
-//   warp 0 lane 0  TMA producer (both CTAs): fills the CTA's own slot and
+// the 192 KB ring is 6 slots deep.  10 warps per CTA:
+//   warp 0         TMA producer (both CTAs): the whole warp runs the loop and
+//                  waits, one elected lane fills the CTA's own slot and
 //                  signals the even CTA's "full" barrier (cta_group::2 copy);
 //   warp 1         allocates 512 TMEM columns for the pair (both CTAs); in the
-//                  even CTA lane 0 issues the paired MMAs into one of two
-//                  256-column fp32 accumulators and releases ring slots and
-//                  accumulators in both CTAs with multicast commits;
+//                  even CTA the whole warp runs the MMA loop and one elected
+//                  lane issues the paired MMAs into one of two 256-column fp32
+//                  accumulators and releases ring slots and accumulators in
+//                  both CTAs with multicast commits;
 //   warps 2..9     epilogue (both CTAs): two warps per TMEM lane quadrant
 //                  (warp % 4), each taking half of the 256 columns, 32 at a
 //                  time (C, when given, is loaded for the whole tile before
@@ -42,6 +57,9 @@
 //                  written with bulk tensor stores (chunks on the diagonal of
 //                  a symmetric result are written element by element); then
 //                  they tell the even CTA that the accumulator is free.
+// Running the producer and MMA loops on whole warps keeps their loop state
+// warp-uniform; a single-lane loop (`if (lane == 0)`) measured 3-18 % slower
+// once its body branched between copy shapes.
 // Every mbarrier wait is bounded (about one second of %globaltimer); a wait
 // that runs out sets a bit in the device status word and the CTA winds down:
 // the issuing CTA waits (bounded) for its MMAs, both CTAs meet at a cluster
@@ -79,6 +97,8 @@ struct GemmParams {
   __half* outT; long long outT_bs; int ld_outT;
   int tma_out, tma_outT;     // the output has a TMA store map (16-byte pitch rules hold)
   int batch, reverse;        // visit matrices from the last one when reverse
+  int a_half, b_half;        // A / B is a half-stored symmetric matrix (M == K / N == K)
+  int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
   unsigned* status;
 };
 
@@ -130,6 +150,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
   }
   return true;
+}
+
+// The same wait by a whole warp: true only if every lane saw the phase.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, unsigned* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+// One lane of a fully active warp (the same lane every time: the lowest).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0u;
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
@@ -271,6 +307,23 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand tile of 128 rows (M or N) x 64 K written by
+// TMA as two 64 x 64 boxes with 128-byte swizzling: each box holds 64 K rows of
+// 128 bytes (64 elements along M/N); 8-row K groups 1024 bytes apart
+// (stride-dimension offset) and the two 64-element M/N halves 8192 bytes apart
+// (leading-dimension offset).  One K = 16 step spans two K groups: 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+constexpr uint32_t kIdescATransposed = 1u << 15;  // A is MN-major
+constexpr uint32_t kIdescBTransposed = 1u << 16;  // B is MN-major
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B both fp16
 // (bits 7-9, 10-12 = 0) or both bf16 (= 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28; M = 256 for the paired MMA (128
@@ -350,6 +403,43 @@ struct Smem {
   static constexpr int kDyn = 1024 + kRingBytes + kStagingBytes + kBarBytes + 16;
 };
 
+// First K slab (of BK) of a half-stored operand whose rows lie in super-row
+// `blk` that must be read from the transpose: the slabs right of its diagonal
+// 256 x 256 block.  nkb (never) for a fully stored operand.
+__device__ __forceinline__ int first_transposed_slab(int half, int blk, int nkb) {
+  const int t = 4 * (blk + 1);
+  return half && t < nkb ? t : nkb;
+}
+
+// MMA issue for K slabs [kb0, kb1) of one tile, A / B K-major or MN-major
+// (AT / BT), run by a whole warp: wait for each ring slot, then one elected
+// lane (always the same, so its commits track all its MMAs) issues four
+// K = 16 paired MMAs and releases the slot in both CTAs.  One K = 16 step advances a descriptor's start address
+// (16-byte units) by 32 bytes along a K-major row, or by two 1024-byte K
+// groups MN-major.  Returns false if a wait ran out.
+template <bool BF16, bool AT, bool BT>
+__device__ __forceinline__ bool mma_slabs(int kb0, int kb1, uint32_t& kc, uint32_t d, uint32_t sA, uint32_t sB,
+                                          uint32_t bar_full, uint32_t bar_empty, unsigned* status) {
+  constexpr uint32_t id = idesc_f32acc<BF16>() | (AT ? kIdescATransposed : 0u) | (BT ? kIdescBTransposed : 0u);
+  constexpr uint64_t a_step = AT ? 128u : 2u, b_step = BT ? 128u : 2u;
+  for (int kb = kb0; kb < kb1; ++kb, ++kc) {
+    const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
+    if (!mbar_wait_warp(bar_full + 8 * s, ph, status)) return false;
+    tc_fence_after();
+    const uint32_t a_src = sA + s * Smem::kABytes, b_src = sB + s * Smem::kBBytes;
+    const uint64_t da = AT ? sdesc_mnmajor_sw128(a_src) : sdesc_kmajor_sw128(a_src);
+    const uint64_t db = BT ? sdesc_mnmajor_sw128(b_src) : sdesc_kmajor_sw128(b_src);
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk)
+        mma_f16_pair(d, da + a_step * kk, db + b_step * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_pair(bar_empty + 8 * s, 0x3);
+    }
+    __syncwarp();
+  }
+  return true;
+}
+
 // Values of one 32-row x 32-column chunk held by a warp: thread `lane` owns
 // row r; v[j] is column c0 + j of the fp32 accumulator.  hp receives
 // alpha D + beta C + gamma I as packed fp16 pairs (rows r >= M give zeros and
@@ -413,9 +503,10 @@ __device__ __forceinline__ uint16_t half_bits(const uint32_t (&hp)[16], int j) {
 
 // Element-wise stores of one chunk: chunks on the diagonal of a symmetric
 // result (an element is kept when r >= c and mirrored when r > c), or outputs
-// whose pitch a TMA map cannot describe.  row0 is the warp's first row.
+// whose pitch a TMA map cannot describe.  row0 is the warp's first row;
+// mirror = false skips the mirror of a symmetric result.
 __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx, int r, int c0, int row0,
-                                                   const uint32_t (&hp)[16]) {
+                                                   const uint32_t (&hp)[16], bool mirror) {
   if (r >= p.M) return;
   const bool sym = p.mode == kSymLower;
   const bool full = (c0 + 32 <= p.N);
@@ -433,7 +524,8 @@ __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx
         if (c0 + j < p.N && (!sym || r >= c0 + j)) dst[j] = __ushort_as_half(half_bits(hp, j));
     }
   }
-  __half* tb = sym ? outb : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
+  __half* tb = sym ? (mirror ? outb : nullptr)
+                    : (p.outT ? p.outT + static_cast<long long>(bidx) * p.outT_bs : nullptr);
   if (tb != nullptr) {
     const int ldt = sym ? p.ld_out : p.ld_outT;
 #pragma unroll
@@ -447,6 +539,7 @@ __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmAT, const __grid_constant__ CUtensorMap tmBT,
                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutT,
                         const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -492,8 +585,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
+    {
+      // ---------------- TMA producer: the whole warp runs the loop, one
+      // elected lane issues the copies ----------------
       uint32_t kc = 0;
       bool ok = true;
       for (int u = cluster; u < p.total_units && ok; u += nclusters) {
@@ -501,17 +595,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int P, bc;
         unit_coords(p, u % p.units_per_mat, P, bc);
         const int bi = 2 * P + static_cast<int>(rank);
+        const int b_row = bc * BN + static_cast<int>(rank) * (BN / 2);
+        const int a_t0 = first_transposed_slab(p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_half, bc, nkb);
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, p.status)) {
+          if (!mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, p.status)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Smem::kStageBytes);
-          const uint32_t full_even = map_to_rank(bar_full + 8 * s, 0);
-          tma_load_3d_pair(sA + s * Smem::kABytes, &tmA, full_even, kb * BK, bi * BM, bidx);
-          tma_load_3d_pair(sB + s * Smem::kBBytes, &tmB, full_even, kb * BK,
-                           bc * BN + static_cast<int>(rank) * (BN / 2), bidx);
+          // An operand tile is one 128-row box of the operand's rows (K-major)
+          // or, for a K range above the diagonal of a half-stored operand, two
+          // 64 x 64 boxes of its transpose: K rows x M/N columns (MN-major).
+          // Coordinates are (column, row, matrix).
+          const uint32_t a_dst = sA + s * Smem::kABytes, b_dst = sB + s * Smem::kBBytes;
+          const int am = bi * BM, k0 = kb * BK;
+          if (elect_one()) {
+            if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Smem::kStageBytes);
+            const uint32_t full_even = map_to_rank(bar_full + 8 * s, 0);
+            if (kb >= a_t0) {
+              tma_load_3d_pair(a_dst, &tmAT, full_even, am, k0, bidx);
+              tma_load_3d_pair(a_dst + Smem::kABytes / 2, &tmAT, full_even, am + BM / 2, k0, bidx);
+            } else {
+              tma_load_3d_pair(a_dst, &tmA, full_even, k0, am, bidx);
+            }
+            if (kb >= b_t0) {
+              tma_load_3d_pair(b_dst, &tmBT, full_even, b_row, k0, bidx);
+              tma_load_3d_pair(b_dst + Smem::kBBytes / 2, &tmBT, full_even, b_row + BN / 4, k0, bidx);
+            } else {
+              tma_load_3d_pair(b_dst, &tmB, full_even, k0, b_row, bidx);
+            }
+          }
+          __syncwarp();
         }
       }
       // Wait (bounded) until every copy issued into the ring has landed, so no
@@ -519,39 +634,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // the bytes of both CTAs).
       for (uint32_t i = 0; leader && i < kStages && i < kc; ++i) {
         const uint32_t last = kc - 1 - i;  // most recent fill of stage last % kStages
-        mbar_wait(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
+        mbar_wait_warp(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_f32acc<BF16>();
+    if (leader) {
+      // ---------------- MMA issuer: the whole warp of the even CTA runs the
+      // loop, one elected lane issues ----------------
       uint32_t kc = 0, tc = 0;
       bool ok = true;
       for (int u = cluster; u < p.total_units && ok; u += nclusters, ++tc) {
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
+        int P, bc;
+        unit_coords(p, u % p.units_per_mat, P, bc);
+        const int a_t0 = first_transposed_slab(p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_half, bc, nkb);
+        if (!mbar_wait_warp(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
-          if (!mbar_wait(bar_full + 8 * s, ph, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t da = sdesc_kmajor_sw128(sA + s * Smem::kABytes);
-          const uint64_t db = sdesc_kmajor_sw128(sB + s * Smem::kBBytes);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_f16_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_pair(bar_empty + 8 * s, kPair);
-        }
-        mma_commit_pair(bar_tfull + 8 * acc, kPair);
+        // K slabs in up to three ranges of fixed operand orientation.
+        const int t1 = a_t0 < b_t0 ? a_t0 : b_t0, t2 = a_t0 < b_t0 ? b_t0 : a_t0;
+        ok = mma_slabs<BF16, false, false>(0, t1, kc, d, sA, sB, bar_full, bar_empty, p.status);
+        if (ok)
+          ok = a_t0 <= b_t0 ? mma_slabs<BF16, true, false>(t1, t2, kc, d, sA, sB, bar_full, bar_empty, p.status)
+                            : mma_slabs<BF16, false, true>(t1, t2, kc, d, sA, sB, bar_full, bar_empty, p.status);
+        if (ok) ok = mma_slabs<BF16, true, true>(t2, nkb, kc, d, sA, sB, bar_full, bar_empty, p.status);
+        if (!ok) break;
+        if (elect_one()) mma_commit_pair(bar_tfull + 8 * acc, kPair);
+        __syncwarp();
       }
-      // All MMAs issued by this thread complete before TMEM is freed.
-      mma_commit_pair(bar_drain, 0x1);
-      mbar_wait(bar_drain, 0u, p.status);
+      // All MMAs issued by the elected lane complete before TMEM is freed.
+      if (elect_one()) mma_commit_pair(bar_drain, 0x1);
+      __syncwarp();
+      mbar_wait_warp(bar_drain, 0u, p.status);
     }
   } else {
     // ---------------- epilogue warps 2 .. 2 + kEpiWarps - 1 ----------------
@@ -563,8 +678,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
     // of a symmetric result, or outT).
     const bool want_n = p.out != nullptr;
-    const bool want_t = sym || p.outT != nullptr;
-    const bool tma_ok = (!want_n || p.tma_out) && (!want_t || (sym ? p.tma_out : p.tma_outT));
+    const bool want_t_any = sym || p.outT != nullptr;
+    const bool tma_ok = (!want_n || p.tma_out) && (!want_t_any || (sym ? p.tma_out : p.tma_outT));
     const CUtensorMap* map_t = sym ? &tmOut : &tmOutT;
     uint32_t staged = 0;  // chunks this warp has staged
     uint32_t tc = 0;
@@ -574,6 +689,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       unit_coords(p, u % p.units_per_mat, P, bc);
       const int bi = 2 * P + static_cast<int>(rank);
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+      // The transposed box of this tile: outT, or the mirror of a symmetric
+      // result (a half-stored one is mirrored on the diagonal super-tiles only).
+      const bool want_t = sym ? (!p.out_half || P == bc) : p.outT != nullptr;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
       // C of every chunk this warp will write (registers; unused entries stay
@@ -602,7 +720,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t hp[16];
         chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
         if (!tma_ok || (sym && row0 <= c0 + 31)) {
-          store_chunk_scalar(p, bidx, r, c0, row0, hp);
+          store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
           continue;
         }
         // Stage the box (and its transpose) in swizzled shared memory, then
@@ -748,6 +866,9 @@ bool gemm_check(const GemmDesc& g, const char** why) {
   if (g.mode == kRect && g.out == nullptr && g.outT == nullptr) return fail("gemm: no output");
   if (g.M > (1 << 24) || g.N > (1 << 24)) return fail("gemm: dimension too large");
   if (g.elem != kF16 && g.elem != kBF16) return fail("gemm: element type must be fp16 or bf16");
+  if (g.a_half && g.M != g.K) return fail("gemm: a half-stored symmetric A needs M == K");
+  if (g.b_half && g.N != g.K) return fail("gemm: a half-stored symmetric B needs N == K");
+  if (g.out_half && g.mode != kSymLower) return fail("gemm: a half-stored output needs the symmetric mode");
   return true;
 }
 
@@ -764,9 +885,14 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   });
   if (attr_err != cudaSuccess) return attr_err;
 
-  CUtensorMap ta, tb;
+  // Operand maps: 128-row boxes for K-major tiles, and 64 x 64 boxes of the
+  // same matrices for the MN-major tiles of half-stored operands (built for
+  // every launch, so the kernel never sees an unset map).
+  CUtensorMap ta, tb, tat, tbt;
   if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM, dt)) return cudaErrorInvalidValue;
   if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tat, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BK, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tbt, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BK, dt)) return cudaErrorInvalidValue;
 
   CUtensorMap to, tt;
   memset(&to, 0, sizeof to);
@@ -814,11 +940,14 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.tma_outT = tma_outT;
   p.batch = g.batch;
   p.reverse = g.reverse ? 1 : 0;
+  p.a_half = g.a_half ? 1 : 0;
+  p.b_half = g.b_half ? 1 : 0;
+  p.out_half = g.out_half ? 1 : 0;
   p.status = dev_status;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;
-  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, to, tt, p);
+  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, tat, tbt, to, tt, p);
   return cudaGetLastError();
 }
 

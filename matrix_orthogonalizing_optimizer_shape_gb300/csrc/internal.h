@@ -117,6 +117,11 @@ struct GemmDesc {
   // previous one wrote last (still in L2).
   bool reverse = false;
   int elem = kF16;  // operand / output element type: kF16 or kBF16 (16-bit storage either way)
+  // Half-stored symmetric matrices (s x s): only the 256 x 256 blocks below the
+  // diagonal and the full diagonal blocks are valid.  a_half / b_half: the
+  // operand is one (M == K / N == K); out_half (kSymLower): write the result
+  // as one (no mirror outside the diagonal super-tiles).
+  bool a_half = false, b_half = false, out_half = false;
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

@@ -1,0 +1,113 @@
+"""Half-stored symmetric matrices in the tcgen05 GEMM (the DION3_GEMM_*_HALF
+mode flags): only the 256 x 256 blocks below the block diagonal and the full
+diagonal blocks hold values.  Products that read such operands (the K ranges
+above the diagonal come from the transpose, as MN-major tiles) must equal the
+products of the fully stored matrices; the region above the diagonal blocks is
+filled with NaN so that any read of it shows.  A half-stored result must equal
+the full result wherever it is defined, and leave the rest untouched."""
+import numpy as np
+import pytest
+import torch
+
+import matrix_orthogonalizing_optimizer_shape_gb300 as d3
+from tests._harness import rel_fro
+
+pytestmark = pytest.mark.gpu
+
+SYM_HALF = d3.GEMM_SYM_LOWER | d3.GEMM_OUT_HALF | d3.GEMM_A_HALF | d3.GEMM_B_HALF
+
+
+def _half_mask(s):
+    """True where a half-stored s x s matrix is defined."""
+    blk = np.arange(s) // 256
+    return blk[:, None] >= blk[None, :]
+
+
+def _sym(rng, batch, s, scale):
+    x = rng.standard_normal((batch, s, s)) * scale
+    return (x + np.swapaxes(x, 1, 2)) / 2
+
+
+def _dev(x, ld=None):
+    b, r, c = x.shape
+    ld = ld or (c + 7) // 8 * 8
+    t = torch.full((b, r, ld), float("nan"), dtype=torch.float16, device="cuda")
+    t[:, :, :c] = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to("cuda").half()
+    return t
+
+
+def _as_half_stored(t, s):
+    """The same device matrices with NaN outside the half-stored region."""
+    h = t.clone()
+    m = torch.from_numpy(~_half_mask(s)).to("cuda")
+    h[:, :s, :s][:, m] = float("nan")
+    return h
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("s,batch", [(200, 3), (256, 2), (512, 2), (700, 2), (1024, 1)])
+def test_half_operands_and_output_match_full(cuda_lib, s, batch):
+    rng = np.random.default_rng(s + 17 * batch)
+    R = _dev(_sym(rng, batch, s, 1.0 / np.sqrt(s)))
+    Cm = _dev(_sym(rng, batch, s, 0.3))
+    a, b, c = d3.MUON_QUINTIC
+    full = _dev(np.zeros((batch, s, s)))
+    d3.gemm_f16(R[:, :, :s], R[:, :, :s], D=full[:, :, :s], C=Cm[:, :, :s], mode=d3.GEMM_SYM_LOWER,
+                alpha=c, beta=b, gamma=a)
+    Rh, Ch = _as_half_stored(R, s), _as_half_stored(Cm, s)
+    out = _dev(np.full((batch, s, s), 7.0))
+    d3.gemm_f16(Rh[:, :, :s], Rh[:, :, :s], D=out[:, :, :s], C=Ch[:, :, :s], mode=SYM_HALF,
+                alpha=c, beta=b, gamma=a)
+    torch.cuda.synchronize()
+    mask = _half_mask(s)
+    got, ref = _np(out[:, :, :s]), _np(full[:, :, :s])
+    assert np.isfinite(got[:, mask]).all()
+    # Same fp16 operand values, same accumulation: the results agree to the
+    # last bit or within a few fp16 ulps.
+    assert np.abs(got[:, mask] - ref[:, mask]).max() <= 4e-3 * max(1.0, np.abs(ref).max())
+    # Outside the diagonal blocks nothing above them was written.
+    assert (got[:, ~mask] == 7.0).all()
+    # The diagonal blocks are exactly symmetric.
+    for b0 in range(0, s, 256):
+        blk = got[:, b0:b0 + 256, b0:b0 + 256]
+        assert np.array_equal(blk, np.swapaxes(blk, 1, 2))
+    # And against float64 on the fp16 operands.
+    R64, C64 = _np(R[:, :, :s]), _np(Cm[:, :, :s])
+    want = c * R64 @ R64 + b * C64 + a * np.eye(s)
+    assert rel_fro(np.where(mask, got, 0), np.where(mask, want, 0)) < 2e-3
+
+
+@pytest.mark.parametrize("L,s,batch", [(1000, 520, 2), (4096, 1024, 1), (300, 700, 2)])
+def test_rect_with_half_stored_b(cuda_lib, L, s, batch):
+    rng = np.random.default_rng(L + s)
+    Yt = _dev(rng.standard_normal((batch, L, s)) / np.sqrt(s))
+    Q = _dev(_sym(rng, batch, s, 1.0 / np.sqrt(s)))
+    D1 = _dev(np.zeros((batch, L, s)))
+    DT1 = _dev(np.zeros((batch, s, L)))
+    d3.gemm_f16(Yt[:, :, :s], Q[:, :, :s], D=D1[:, :, :s], DT=DT1[:, :, :L], mode=d3.GEMM_RECT)
+    Qh = _as_half_stored(Q, s)
+    D2 = _dev(np.zeros((batch, L, s)))
+    DT2 = _dev(np.zeros((batch, s, L)))
+    d3.gemm_f16(Yt[:, :, :s], Qh[:, :, :s], D=D2[:, :, :s], DT=DT2[:, :, :L],
+                mode=d3.GEMM_RECT | d3.GEMM_B_HALF)
+    torch.cuda.synchronize()
+    g1, g2 = _np(D1[:, :, :s]), _np(D2[:, :, :s])
+    assert np.isfinite(g2).all()
+    assert np.abs(g2 - g1).max() <= 4e-3 * max(1.0, np.abs(g1).max())
+    assert np.array_equal(_np(DT2[:, :, :L]), np.swapaxes(g2, 1, 2))
+    want = _np(Yt[:, :, :s]) @ _np(Q[:, :, :s])
+    assert rel_fro(g2, want) < 2e-3
+
+
+def test_half_flag_rules(cuda_lib):
+    A = torch.zeros((1, 256, 128), dtype=torch.float16, device="cuda")
+    D = torch.zeros((1, 256, 256), dtype=torch.float16, device="cuda")
+    with pytest.raises(d3.Dion3Error):   # A_HALF needs M == K
+        d3.gemm_f16(A, A, D=D, mode=d3.GEMM_SYM_LOWER | d3.GEMM_A_HALF)
+    with pytest.raises(d3.Dion3Error):   # OUT_HALF needs the symmetric mode
+        d3.gemm_f16(A, A, D=D, mode=d3.GEMM_RECT | d3.GEMM_OUT_HALF)
+    with pytest.raises(d3.Dion3Error):   # unknown flag
+        d3.gemm_f16(A, A, D=D, mode=d3.GEMM_SYM_LOWER | 0x100)
