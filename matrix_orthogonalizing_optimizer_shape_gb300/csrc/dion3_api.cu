@@ -447,6 +447,8 @@ dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const Ns
     g1.B = p.Y[cur]; g1.b_bstride = p.y_bs; g1.ldb = p.Lp;
     g1.M = p.s; g1.N = p.s; g1.K = p.L; g1.batch = p.batch;
     g1.mode = mode_sym; g1.alpha = 1.f;
+    // The symmetric s x s matrices are half-stored, as in the Gram schedule.
+    g1.out_half = !dense;
     g1.out = p.S[0]; g1.out_bstride = p.s_bs; g1.ld_out = p.sp;
     if ((rc = launch(g1)) != DION3_OK) return rc;
     // B = c A.A + b A
@@ -455,6 +457,7 @@ dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const Ns
     g2.B = p.S[0]; g2.b_bstride = p.s_bs; g2.ldb = p.sp;
     g2.M = p.s; g2.N = p.s; g2.K = p.s; g2.batch = p.batch;
     g2.mode = mode_sym; g2.alpha = hp.c; g2.beta = hp.b;
+    g2.a_half = g2.b_half = g2.out_half = !dense;
     g2.C = p.S[0]; g2.c_bstride = p.s_bs; g2.ldc = p.sp;
     g2.out = p.S[1]; g2.out_bstride = p.s_bs; g2.ld_out = p.sp;
     if ((rc = launch(g2)) != DION3_OK) return rc;
@@ -464,6 +467,7 @@ dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const Ns
     g3.B = p.Yt[cur]; g3.b_bstride = p.yt_bs; g3.ldb = p.sp;
     g3.M = p.s; g3.N = p.L; g3.K = p.s; g3.batch = p.batch;
     g3.mode = kRect; g3.alpha = 1.f; g3.beta = hp.a;
+    g3.a_half = !dense;
     g3.C = p.Y[cur]; g3.c_bstride = p.y_bs; g3.ldc = p.Lp;
     if (!last) {
       g3.out = p.Y[nxt]; g3.out_bstride = p.y_bs; g3.ld_out = p.Lp;
