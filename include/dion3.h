@@ -217,8 +217,14 @@ typedef enum { DION3_GEMM_RECT = 0, DION3_GEMM_SYM_LOWER = 1 } dion3_gemm_mode;
  *   DION3_GEMM_A_HALF:   A is half-stored (needs M == K); the part of A above
  *                        the diagonal blocks is read from its transpose.
  *   DION3_GEMM_B_HALF:   B is half-stored (needs N == K), likewise.
+ * and for operands given as their transpose:
+ *   DION3_GEMM_A_TRANS:  A is passed as A^T, stored [batch][K][M] with pitch
+ *                        lda >= M (so V = alpha (A^T)^T B^T + ...);
+ *   DION3_GEMM_B_TRANS:  B is passed as B^T, stored [batch][K][N], ldb >= N.
+ * An operand cannot be both transposed and half-stored.
  */
-enum { DION3_GEMM_OUT_HALF = 0x10, DION3_GEMM_A_HALF = 0x20, DION3_GEMM_B_HALF = 0x40 };
+enum { DION3_GEMM_OUT_HALF = 0x10, DION3_GEMM_A_HALF = 0x20, DION3_GEMM_B_HALF = 0x40,
+       DION3_GEMM_A_TRANS = 0x100, DION3_GEMM_B_TRANS = 0x200 };
 
 /*
  * The tensor-core GEMM behind step (b), callable on its own.  Second-level
@@ -238,8 +244,8 @@ enum { DION3_GEMM_OUT_HALF = 0x10, DION3_GEMM_A_HALF = 0x20, DION3_GEMM_B_HALF =
  *                         A B^T is symmetric: A == B, or A and B commuting
  *                         symmetric matrices (then B^T = B).
  *   The mode may carry the DION3_GEMM_*_HALF flags above.
- * Rules: A and B 16-byte aligned; lda, ldb >= K and multiples of 8; their batch
- * strides multiples of 8.  D, DT and C may have any pitch >= their row length.
+ * Rules: A and B 16-byte aligned; lda, ldb >= K (>= M / N when transposed) and
+ * multiples of 8; their batch strides multiples of 8.  D, DT and C may have any pitch >= their row length.
  * An unknown mode or flag, or a flag whose shape rule does not hold, returns
  * DION3_ERR_INVALID_ARG with nothing launched.
  */

@@ -341,21 +341,24 @@ GEMM_RECT, GEMM_SYM_LOWER = 0, 1
 #: 256 x 256 blocks below the block diagonal and the full diagonal blocks hold
 #: valid values.
 GEMM_OUT_HALF, GEMM_A_HALF, GEMM_B_HALF = 0x10, 0x20, 0x40
+#: Mode flags for operands passed as their transpose (A stored [K][M], B [K][N]).
+GEMM_A_TRANS, GEMM_B_TRANS = 0x100, 0x200
 
 
 def gemm_f16(A, B, D=None, DT=None, C=None, *, mode: int = GEMM_RECT, alpha: float = 1.0,
              beta: float = 0.0, gamma: float = 0.0, stream=None):
     """V = alpha A B^T + beta C + gamma I on fp16 [batch, rows, cols] tensors
     (see dion3_gemm_f16); 2-D tensors are a batch of one.  Pitches and batch
-    strides are taken from the tensors' strides."""
+    strides are taken from the tensors' strides.  With GEMM_A_TRANS (GEMM_B_TRANS)
+    in `mode`, the tensor passed as A (B) holds A^T (B^T)."""
     def geom(t, rows_dim=-2):
         if t is None:
             return 0, 0, 0
         st = t.stride()
         return _ptr(t), st[-2], (st[0] if t.dim() == 3 else st[-2] * t.shape[-2])
     batch = A.shape[0] if A.dim() == 3 else 1
-    M, K = A.shape[-2], A.shape[-1]
-    N = B.shape[-2]
+    M, K = (A.shape[-1], A.shape[-2]) if mode & GEMM_A_TRANS else (A.shape[-2], A.shape[-1])
+    N = B.shape[-1] if mode & GEMM_B_TRANS else B.shape[-2]
     a, b, c, d, dt = geom(A), geom(B), geom(C), geom(D), geom(DT)
     _check(load_library().dion3_gemm_f16(mode, M, N, K, batch, *a, *b, *c, *d, *dt,
                                          alpha, beta, gamma, _stream(stream)))

@@ -167,13 +167,16 @@ struct Carver {
 
 // Gram-NS buffers for `batch` k x m problems.  Y is the s x L operand (s =
 // min(k, m)); Yt0/Yt1 hold L x s transposes; S[0..3] are s x s buffers.
+// The Gram-NS workspace of one shape group.  The normalised rows are kept in
+// one orientation only, X itself ([batch][k][mp], mp = round_up(m, 8)): when
+// k <= m (wide) that is Y, when k > m it is Y^T.  Products that need the other
+// orientation read it through the GEMM's transposed-operand tiles.
 struct NsPlan {
-  int k, m, batch, s, L, sp, Lp;
-  bool wide;  // k <= m: Y = X; else Y = X^T
-  __half* Y;
-  __half* Yt[2];
-  __half* S[4];
-  long long y_bs, yt_bs, s_bs;
+  int k, m, batch, s, L, sp, mp;
+  bool wide;      // k <= m: Y = X (s x L); else Y = X^T and X is Y^T (L x s)
+  __half* X[2];   // ping-pong for the restart (Y <- Q Y reads one, writes the other)
+  __half* S[4];   // s x s matrices, half-stored symmetric
+  long long x_bs, s_bs;
 };
 
 void plan_ns(Carver& c, int k, int m, int batch, NsPlan& p) {
@@ -184,27 +187,20 @@ void plan_ns(Carver& c, int k, int m, int batch, NsPlan& p) {
   p.s = p.wide ? k : m;
   p.L = p.wide ? m : k;
   p.sp = static_cast<int>(round_up(p.s, 8));
-  p.Lp = static_cast<int>(round_up(p.L, 8));
-  p.y_bs = static_cast<long long>(p.s) * p.Lp;
-  p.yt_bs = static_cast<long long>(p.L) * p.sp;
+  p.mp = static_cast<int>(round_up(m, 8));
+  p.x_bs = static_cast<long long>(k) * p.mp;
   p.s_bs = static_cast<long long>(p.s) * p.sp;
-  p.Y = c.take<__half>(p.y_bs * batch);
-  p.Yt[0] = c.take<__half>(p.yt_bs * batch);
-  p.Yt[1] = c.take<__half>(p.yt_bs * batch);
+  p.X[0] = c.take<__half>(p.x_bs * batch);
+  p.X[1] = c.take<__half>(p.x_bs * batch);
   for (int i = 0; i < 4; ++i) p.S[i] = c.take<__half>(p.s_bs * batch);
 }
 
-// Where the gather kernel writes the two orientations of the normalised rows.
+// Where the gather kernel writes the normalised rows: X[0], rows only.
 void gather_targets(const NsPlan& p, GatherArgs& g) {
-  // Rows orientation: k x m, pitch round_up(m, 8); columns: m x k, pitch
-  // round_up(k, 8).
-  if (p.wide) {
-    g.out_rows = p.Y;      g.rows_bstride = p.y_bs;  g.ld_rows = p.Lp;
-    g.out_cols = p.Yt[0];  g.cols_bstride = p.yt_bs; g.ld_cols = p.sp;
-  } else {
-    g.out_rows = p.Yt[0];  g.rows_bstride = p.yt_bs; g.ld_rows = p.sp;
-    g.out_cols = p.Y;      g.cols_bstride = p.y_bs;  g.ld_cols = p.Lp;
-  }
+  g.out_rows = p.X[0];
+  g.rows_bstride = p.x_bs;
+  g.ld_rows = p.mp;
+  g.out_cols = nullptr;
 }
 
 // Traced launch helpers: the algorithmic work of one launch.
@@ -236,7 +232,7 @@ cudaError_t traced_topk(const TopkArgs& t, cudaStream_t s) {
 }
 cudaError_t traced_gather(const GatherArgs& g, bool vec, cudaStream_t s) {
   const double per = g.src_f32 ? (4.0 + (g.decay ? 4.0 : 0.0)) : 2.0;
-  const double bytes = static_cast<double>(g.batch) * g.k * g.m * (per + 4.0);
+  const double bytes = static_cast<double>(g.batch) * g.k * g.m * (per + (g.out_cols != nullptr ? 4.0 : 2.0));
   return traced("gather_normalize", 0.0, bytes, s, [&] { return launch_gather(g, vec, s); });
 }
 cudaError_t traced_sumsq(const __half* X, long long n, int batch, float* parts, int nparts, bool bf16,
@@ -286,13 +282,23 @@ struct NsOut {
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
                          cudaStream_t stream, bool dense = false) {
-  auto sym = [&](const __half* A, const __half* B, __half* D, int K, const __half* C, float alpha, float beta,
-                 float gamma, const __half* Abase_is_Y) -> GemmDesc {
+  // Symmetric product of two s x s matrices (or, with xi >= 0, the SYRK
+  // R = Y Y^T from X[xi]: Y itself when wide, given as its transpose X = Y^T
+  // otherwise).
+  auto sym = [&](const __half* A, const __half* B, __half* D, const __half* C, float alpha, float beta,
+                 float gamma, int xi = -1) -> GemmDesc {
     GemmDesc g{};
-    const bool from_y = Abase_is_Y != nullptr;
-    g.A = A; g.a_bstride = from_y ? p.y_bs : p.s_bs; g.lda = from_y ? p.Lp : p.sp;
-    g.B = B; g.b_bstride = from_y ? p.y_bs : p.s_bs; g.ldb = from_y ? p.Lp : p.sp;
-    g.M = p.s; g.N = p.s; g.K = K; g.batch = p.batch;
+    const bool from_y = xi >= 0;
+    if (from_y) {
+      g.A = g.B = p.X[xi];
+      g.a_bstride = g.b_bstride = p.x_bs;
+      g.lda = g.ldb = p.mp;
+      g.a_tr = g.b_tr = !p.wide;
+    } else {
+      g.A = A; g.a_bstride = p.s_bs; g.lda = p.sp;
+      g.B = B; g.b_bstride = p.s_bs; g.ldb = p.sp;
+    }
+    g.M = p.s; g.N = p.s; g.K = from_y ? p.L : p.s; g.batch = p.batch;
     // dense: every tile of the product (the comparison path without the
     // symmetric savings); otherwise lower-triangle tiles.  Every s x s matrix
     // of the chain is then half-stored (the 256 x 256 blocks below the block
@@ -328,51 +334,57 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
       if (i != a && i != b && i != c) return i;
     return -1;
   };
-  int ycur = 0;  // Yt[ycur] is the current Y^T
+  int xcur = 0;  // X[xcur] holds the current Y (wide) or Y^T
+  // D = Y^T Q (L x s): A = Y^T is X[xcur] itself (k > m) or given as its
+  // transpose (wide); B = Q half-stored.
+  auto rect_ytq = [&](int xi) -> GemmDesc {
+    GemmDesc g{};
+    g.A = p.X[xi]; g.a_bstride = p.x_bs; g.lda = p.mp;
+    g.a_tr = p.wide;
+    g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
+    g.b_half = !dense;
+    g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
+    g.mode = kRect; g.alpha = 1.f;
+    return g;
+  };
 
   // R = Y Y^T
-  if ((rc = launch(sym(p.Y, p.Y, p.S[R], p.L, nullptr, 1.f, 0.f, 0.f, p.Y))) != DION3_OK) return rc;
+  if ((rc = launch(sym(nullptr, nullptr, p.S[R], nullptr, 1.f, 0.f, 0.f, xcur))) != DION3_OK) return rc;
   const int T = hp.ns_steps, rs = hp.restart_iter;
   for (int t = 1; t <= T; ++t) {
     if (rs > 1 && t == rs) {
-      // Y <- Q Y:  D = Y^T Q (L x s) is the new Y^T; its transpose the new Y.
-      GemmDesc g{};
-      g.A = p.Yt[ycur]; g.a_bstride = p.yt_bs; g.lda = p.sp;
-      g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
-      g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
-      g.mode = kRect; g.alpha = 1.f;
-      g.b_half = !dense;
-      g.out = p.Yt[ycur ^ 1]; g.out_bstride = p.yt_bs; g.ld_out = p.sp;
-      g.outT = p.Y; g.outT_bstride = p.y_bs; g.ld_outT = p.Lp;
+      // Y <- Q Y:  D = Y^T Q (L x s) is the new Y^T; stored in X's
+      // orientation: D^T = the new Y when wide, D itself otherwise.
+      GemmDesc g = rect_ytq(xcur);
+      if (p.wide) {
+        g.outT = p.X[xcur ^ 1]; g.outT_bstride = p.x_bs; g.ld_outT = p.mp;
+      } else {
+        g.out = p.X[xcur ^ 1]; g.out_bstride = p.x_bs; g.ld_out = p.mp;
+      }
       if ((rc = launch(g)) != DION3_OK) return rc;
-      ycur ^= 1;
-      if ((rc = launch(sym(p.Y, p.Y, p.S[R], p.L, nullptr, 1.f, 0.f, 0.f, p.Y))) != DION3_OK) return rc;
+      xcur ^= 1;
+      if ((rc = launch(sym(nullptr, nullptr, p.S[R], nullptr, 1.f, 0.f, 0.f, xcur))) != DION3_OK) return rc;
       Q = -1;
     }
     // Z = c R.R + b R + a I
     Z = free_buf(R, Q, -1);
-    if ((rc = launch(sym(p.S[R], p.S[R], p.S[Z], p.s, p.S[R], hp.c, hp.b, hp.a, nullptr))) != DION3_OK) return rc;
+    if ((rc = launch(sym(p.S[R], p.S[R], p.S[Z], p.S[R], hp.c, hp.b, hp.a))) != DION3_OK) return rc;
     if (Q < 0) {
       Q = Z;  // Q <- Z
     } else {
       const int nq = free_buf(R, Q, Z);
-      if ((rc = launch(sym(p.S[Z], p.S[Q], p.S[nq], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
+      if ((rc = launch(sym(p.S[Z], p.S[Q], p.S[nq], nullptr, 1.f, 0.f, 0.f))) != DION3_OK) return rc;
       Q = nq;
     }
     if (t < T && t + 1 != rs) {
       // R <- Z (R Z); Z may be the buffer Q now points at, which is only read.
       const int tm = free_buf(R, Q, Z);
-      if ((rc = launch(sym(p.S[R], p.S[Z], p.S[tm], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
-      if ((rc = launch(sym(p.S[Z], p.S[tm], p.S[R], p.s, nullptr, 1.f, 0.f, 0.f, nullptr))) != DION3_OK) return rc;
+      if ((rc = launch(sym(p.S[R], p.S[Z], p.S[tm], nullptr, 1.f, 0.f, 0.f))) != DION3_OK) return rc;
+      if ((rc = launch(sym(p.S[Z], p.S[tm], p.S[R], nullptr, 1.f, 0.f, 0.f))) != DION3_OK) return rc;
     }
   }
   // O = Q Y, written as X's k x m orientation.
-  GemmDesc g{};
-  g.A = p.Yt[ycur]; g.a_bstride = p.yt_bs; g.lda = p.sp;
-  g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
-  g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
-  g.mode = kRect; g.alpha = 1.f;
-  g.b_half = !dense;
+  GemmDesc g = rect_ytq(xcur);
   if (p.wide) {
     g.outT = out.O; g.outT_bstride = out.o_bs; g.ld_outT = out.ld_o;
   } else {
@@ -916,8 +928,10 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
   const int32_t flags = mode & ~0xF;
   mode &= 0xF;
   if (mode != DION3_GEMM_RECT && mode != DION3_GEMM_SYM_LOWER) return fail(DION3_ERR_INVALID_ARG, "bad GEMM mode");
-  if ((flags & ~(DION3_GEMM_OUT_HALF | DION3_GEMM_A_HALF | DION3_GEMM_B_HALF)) != 0)
+  if ((flags & ~(DION3_GEMM_OUT_HALF | DION3_GEMM_A_HALF | DION3_GEMM_B_HALF | DION3_GEMM_A_TRANS |
+                 DION3_GEMM_B_TRANS)) != 0)
     return fail(DION3_ERR_INVALID_ARG, "unknown GEMM mode flag");
+  const bool a_tr = (flags & DION3_GEMM_A_TRANS) != 0, b_tr = (flags & DION3_GEMM_B_TRANS) != 0;
   if (M < 1 || N < 1 || K < 1 || batch < 1 || batch > 65535)
     return fail(DION3_ERR_INVALID_ARG, "need M, N, K >= 1 and 1 <= batch <= 65535");
   if (mode == DION3_GEMM_SYM_LOWER && (M != N || D == nullptr || DT != nullptr))
@@ -928,7 +942,8 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
   if (C != nullptr && ldc < N) return fail(DION3_ERR_INVALID_ARG, "ldc < N");
   if (((reinterpret_cast<uintptr_t>(D) | reinterpret_cast<uintptr_t>(DT) | reinterpret_cast<uintptr_t>(C)) & 1u) != 0)
     return fail(DION3_ERR_INVALID_ARG, "C, D and DT must be 2-byte aligned");
-  if (batch > 1 && (a_bstride < static_cast<int64_t>(lda) * M || b_bstride < static_cast<int64_t>(ldb) * N))
+  if (batch > 1 && (a_bstride < static_cast<int64_t>(lda) * (a_tr ? K : M) ||
+                    b_bstride < static_cast<int64_t>(ldb) * (b_tr ? K : N)))
     return fail(DION3_ERR_INVALID_ARG, "operand batch stride smaller than one matrix");
   GemmDesc g{};
   g.A = static_cast<const __half*>(A); g.a_bstride = a_bstride; g.lda = lda;
@@ -942,6 +957,8 @@ dion3_status dion3_gemm_f16(int32_t mode, int32_t M, int32_t N, int32_t K, int32
   g.out_half = (flags & DION3_GEMM_OUT_HALF) != 0;
   g.a_half = (flags & DION3_GEMM_A_HALF) != 0;
   g.b_half = (flags & DION3_GEMM_B_HALF) != 0;
+  g.a_tr = a_tr;
+  g.b_tr = b_tr;
   const char* why = nullptr;
   if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "%s", why);
   if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");

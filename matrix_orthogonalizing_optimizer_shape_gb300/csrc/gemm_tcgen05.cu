@@ -20,7 +20,9 @@
 // MN-major bit of the instruction descriptor set.  Both CTAs of a pair have
 // the same 256-row super-row, so they always agree on the orientation.  This
 // skips the mirror writes outside the diagonal blocks and never touches the
-// upper triangle.
+// upper triangle.  The same MN-major tiles read an operand that is given as its
+// transpose (a_tr / b_tr: A stored [K][M]), so a matrix kept in one orientation
+// serves as A = Y or A = Y^T alike.
 //
 // Method source: "Dion3: Full-Stack Orthogonal Updates" (agihunt summary of the
 // paper).  First-level paragraph: Newton-Schulz iterates on the small
@@ -98,6 +100,7 @@ struct GemmParams {
   int tma_out, tma_outT;     // the output has a TMA store map (16-byte pitch rules hold)
   int batch, reverse;        // visit matrices from the last one when reverse
   int a_half, b_half;        // A / B is a half-stored symmetric matrix (M == K / N == K)
+  int a_tr, b_tr;            // A / B is given as its transpose ([K][M] / [K][N]): all tiles MN-major
   int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
   unsigned* status;
 };
@@ -403,10 +406,12 @@ struct Smem {
   static constexpr int kDyn = 1024 + kRingBytes + kStagingBytes + kBarBytes + 16;
 };
 
-// First K slab (of BK) of a half-stored operand whose rows lie in super-row
-// `blk` that must be read from the transpose: the slabs right of its diagonal
-// 256 x 256 block.  nkb (never) for a fully stored operand.
-__device__ __forceinline__ int first_transposed_slab(int half, int blk, int nkb) {
+// First K slab (of BK) of an operand whose rows lie in super-row `blk` that is
+// read from the transpose as MN-major tiles: 0 for an operand given as its
+// transpose; for a half-stored one the slabs right of its diagonal 256 x 256
+// block; nkb (never) for a plain operand.
+__device__ __forceinline__ int first_transposed_slab(int tr, int half, int blk, int nkb) {
+  if (tr) return 0;
   const int t = 4 * (blk + 1);
   return half && t < nkb ? t : nkb;
 }
@@ -596,8 +601,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         unit_coords(p, u % p.units_per_mat, P, bc);
         const int bi = 2 * P + static_cast<int>(rank);
         const int b_row = bc * BN + static_cast<int>(rank) * (BN / 2);
-        const int a_t0 = first_transposed_slab(p.a_half, P, nkb);
-        const int b_t0 = first_transposed_slab(p.b_half, bc, nkb);
+        const int a_t0 = first_transposed_slab(p.a_tr, p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_tr, p.b_half, bc, nkb);
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
           if (!mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, p.status)) {
@@ -647,8 +652,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
         int P, bc;
         unit_coords(p, u % p.units_per_mat, P, bc);
-        const int a_t0 = first_transposed_slab(p.a_half, P, nkb);
-        const int b_t0 = first_transposed_slab(p.b_half, bc, nkb);
+        const int a_t0 = first_transposed_slab(p.a_tr, p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_tr, p.b_half, bc, nkb);
         if (!mbar_wait_warp(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
@@ -861,7 +866,8 @@ bool gemm_check(const GemmDesc& g, const char** why) {
     return fail("gemm: operands must be 16-byte aligned");
   if (g.lda % 8 || g.ldb % 8 || g.a_bstride % 8 || g.b_bstride % 8)
     return fail("gemm: operand pitches must be multiples of 8 elements");
-  if (g.lda < g.K || g.ldb < g.K) return fail("gemm: pitch smaller than K");
+  if (g.lda < (g.a_tr ? g.M : g.K) || g.ldb < (g.b_tr ? g.N : g.K)) return fail("gemm: operand pitch smaller than its row");
+  if ((g.a_tr && g.a_half) || (g.b_tr && g.b_half)) return fail("gemm: an operand is either transposed or half-stored");
   if (g.mode == kSymLower && (g.M != g.N || g.out == nullptr)) return fail("gemm: symmetric mode needs M == N and out");
   if (g.mode == kRect && g.out == nullptr && g.outT == nullptr) return fail("gemm: no output");
   if (g.M > (1 << 24) || g.N > (1 << 24)) return fail("gemm: dimension too large");
@@ -888,11 +894,15 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   // Operand maps: 128-row boxes for K-major tiles, and 64 x 64 boxes of the
   // same matrices for the MN-major tiles of half-stored operands (built for
   // every launch, so the kernel never sees an unset map).
+  // An operand given as its transpose is stored [K][M] (or [K][N]): both of
+  // its maps describe that storage (only the 64 x 64 one is used).
   CUtensorMap ta, tb, tat, tbt;
-  if (!make_map(&ta, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BM, dt)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BN / 2, dt)) return cudaErrorInvalidValue;
-  if (!make_map(&tat, g.A, g.a_bstride, g.lda, g.M, g.K, g.batch, BK, dt)) return cudaErrorInvalidValue;
-  if (!make_map(&tbt, g.B, g.b_bstride, g.ldb, g.N, g.K, g.batch, BK, dt)) return cudaErrorInvalidValue;
+  const int a_rows = g.a_tr ? g.K : g.M, a_cols = g.a_tr ? g.M : g.K;
+  const int b_rows = g.b_tr ? g.K : g.N, b_cols = g.b_tr ? g.N : g.K;
+  if (!make_map(&ta, g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, g.a_tr ? BK : BM, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, g.b_tr ? BK : BN / 2, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tat, g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, BK, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tbt, g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, BK, dt)) return cudaErrorInvalidValue;
 
   CUtensorMap to, tt;
   memset(&to, 0, sizeof to);
@@ -941,6 +951,8 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.batch = g.batch;
   p.reverse = g.reverse ? 1 : 0;
   p.a_half = g.a_half ? 1 : 0;
+  p.a_tr = g.a_tr ? 1 : 0;
+  p.b_tr = g.b_tr ? 1 : 0;
   p.b_half = g.b_half ? 1 : 0;
   p.out_half = g.out_half ? 1 : 0;
   p.status = dev_status;

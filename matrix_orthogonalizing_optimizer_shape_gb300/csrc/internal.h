@@ -63,7 +63,7 @@ struct GatherArgs {
   float* scale_out = nullptr;      // lazy decay: scale_out[b][row] = mu for the selected rows
   unsigned* status;                // device status word (kDevCheck on a bad index)
   __half* out_rows; long long rows_bstride; int ld_rows;   // [k][ld_rows]
-  __half* out_cols; long long cols_bstride; int ld_cols;   // [m][ld_cols]
+  __half* out_cols; long long cols_bstride; int ld_cols;   // [m][ld_cols], or null: rows only
 };
 cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s);
 
@@ -122,6 +122,9 @@ struct GemmDesc {
   // operand is one (M == K / N == K); out_half (kSymLower): write the result
   // as one (no mirror outside the diagonal super-tiles).
   bool a_half = false, b_half = false, out_half = false;
+  // The operand is given as its transpose: A stored [batch][K][M] (lda >= M),
+  // B stored [batch][K][N] (ldb >= N); read as MN-major tiles.
+  bool a_tr = false, b_tr = false;
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

@@ -254,11 +254,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// a2: gather + normalise into fp16, both orientations, with the error-feedback
-// decay of the source momentum rows fused in (the undecayed values are the
-// ones normalised).  Tile: 32 selected rows x 128 columns per CTA; each warp
-// reads one 512-byte row segment per pass; the column-major copy is staged
-// through shared memory so both outputs are written in contiguous runs.
+// a2: gather + normalise into fp16, in the rows orientation and (if out_cols
+// is set) also the columns orientation, with the error-feedback decay of the
+// source momentum rows fused in (the undecayed values are the ones
+// normalised).  Tile: 32 selected rows x 128 columns per CTA; each warp reads
+// one 512-byte row segment per pass; the column-major copy is staged through
+// shared memory so both outputs are written in contiguous runs.
 // ---------------------------------------------------------------------------
 constexpr int kGRows = 32, kGCols = 128;
 
@@ -345,9 +346,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
           if (c + j < a.m) dst[j] = h[j];
       }
     }
+    if (a.out_cols != nullptr) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tile[lane * 4 + j][rr] = h[j];
+      for (int j = 0; j < 4; ++j) tile[lane * 4 + j][rr] = h[j];
+    }
   }
+  if (a.out_cols == nullptr) return;  // CTA-uniform
   __syncthreads();
 
   // Column-major copy: out_cols[c][i0 .. i0+32), 16 bytes per thread.  Rows

@@ -170,7 +170,8 @@ def test_gemm_half_flag_validation(lib):
     def call(mode, M, N, K):
         return lib.dion3_gemm_f16(mode, M, N, K, 1, 0x10000, 256, 65536, 0x20000, 256, 65536,
                                   None, 0, 0, 0x30000, 256, 65536, None, 0, 0, 1.0, 0.0, 0.0, None)
-    assert call(d3.GEMM_SYM_LOWER | 0x80, 256, 256, 256) == d3.ERR_INVALID_ARG    # unknown flag
+    assert call(d3.GEMM_SYM_LOWER | 0x800, 256, 256, 256) == d3.ERR_INVALID_ARG   # unknown flag
+    assert call(d3.GEMM_RECT | d3.GEMM_A_TRANS | d3.GEMM_A_HALF, 256, 256, 256) == d3.ERR_INVALID_ARG  # both
     assert call(d3.GEMM_SYM_LOWER | d3.GEMM_A_HALF, 256, 256, 128) == d3.ERR_INVALID_ARG  # A half needs M == K
     assert call(d3.GEMM_RECT | d3.GEMM_B_HALF, 256, 200, 256) == d3.ERR_INVALID_ARG      # B half needs N == K
     assert call(d3.GEMM_RECT | d3.GEMM_OUT_HALF, 256, 256, 256) == d3.ERR_INVALID_ARG    # needs the symmetric mode

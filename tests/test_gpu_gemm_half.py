@@ -110,4 +110,46 @@ def test_half_flag_rules(cuda_lib):
     with pytest.raises(d3.Dion3Error):   # OUT_HALF needs the symmetric mode
         d3.gemm_f16(A, A, D=D, mode=d3.GEMM_RECT | d3.GEMM_OUT_HALF)
     with pytest.raises(d3.Dion3Error):   # unknown flag
-        d3.gemm_f16(A, A, D=D, mode=d3.GEMM_SYM_LOWER | 0x100)
+        d3.gemm_f16(A, A, D=D, mode=d3.GEMM_SYM_LOWER | 0x800)
+
+
+@pytest.mark.parametrize("M,N,K,batch", [(1000, 520, 520, 2), (300, 700, 1024, 1), (4096, 1024, 1024, 1)])
+def test_transposed_operands_match_plain(cuda_lib, M, N, K, batch):
+    """A (or B) passed as its transpose, read as MN-major tiles, gives the same
+    product as the plain K-major operand."""
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A = _dev(rng.standard_normal((batch, M, K)) / np.sqrt(K))
+    B = _dev(rng.standard_normal((batch, N, K)))
+    # The same fp16 values stored transposed (pitches padded to 8 elements).
+    At = _dev(np.swapaxes(_np(A[:, :, :K]), 1, 2))[:, :, :M]
+    Bt = _dev(np.swapaxes(_np(B[:, :, :K]), 1, 2))[:, :, :N]
+    ref = _dev(np.zeros((batch, M, N)))
+    d3.gemm_f16(A[:, :, :K], B[:, :, :K], D=ref[:, :, :N])
+    for mode, a, b in [(d3.GEMM_A_TRANS, At, B[:, :, :K]), (d3.GEMM_B_TRANS, A[:, :, :K], Bt),
+                       (d3.GEMM_A_TRANS | d3.GEMM_B_TRANS, At, Bt)]:
+        D = _dev(np.zeros((batch, M, N)))
+        DT = _dev(np.zeros((batch, N, M)))
+        d3.gemm_f16(a, b, D=D[:, :, :N], DT=DT[:, :, :M], mode=d3.GEMM_RECT | mode)
+        torch.cuda.synchronize()
+        got, want = _np(D[:, :, :N]), _np(ref[:, :, :N])
+        assert np.isfinite(got).all()
+        assert np.abs(got - want).max() <= 4e-3 * max(1.0, np.abs(want).max()), mode
+        assert np.array_equal(_np(DT[:, :, :M]), np.swapaxes(got, 1, 2))
+
+
+def test_syrk_from_transposed_storage(cuda_lib):
+    """R = Y Y^T with Y given as its transpose (the k > m case of the Gram
+    path), written half-stored."""
+    rng = np.random.default_rng(5)
+    batch, s, L = 2, 700, 1500
+    Yt = _dev(rng.standard_normal((batch, L, s)) / np.sqrt(L))      # stored Y^T, [L][s]
+    R = _dev(np.full((batch, s, s), 7.0))
+    d3.gemm_f16(Yt[:, :, :s], Yt[:, :, :s], D=R[:, :, :s],
+                mode=d3.GEMM_SYM_LOWER | d3.GEMM_OUT_HALF | d3.GEMM_A_TRANS | d3.GEMM_B_TRANS)
+    torch.cuda.synchronize()
+    Y = np.swapaxes(_np(Yt[:, :, :s]), 1, 2)
+    want = Y @ np.swapaxes(Y, 1, 2)
+    mask = _half_mask(s)
+    got = _np(R[:, :, :s])
+    assert (got[:, ~mask] == 7.0).all()
+    assert rel_fro(np.where(mask, got, 0), np.where(mask, want, 0)) < 2e-3
