@@ -19,6 +19,7 @@ Printed (rank 0, one JSON line):
                peak in MEASURED_PEAKS.json.
   cpu_baseline the float64 CPU oracle timed on a bounded sample (one matrix of
                each shape group) and scaled to the full set.
+  graph        the same step captured once in a CUDA graph and replayed.
   per_model    (default workload only) step ms and useful TFLOP/s with their
                fraction of the measured bf16 peak for each model at each f:
                7B at f = 1/4 (the headline) and 1/8, 1B at f = 1, 1/2, 1/4.
@@ -342,6 +343,36 @@ def run_ours(args, rank, world, device_index):
     ms_max = max_over_ranks(ms, world, device)
     launches = sum(v["launches"] for v in trace.values())
 
+    # The same step captured once in a CUDA graph and replayed K times: no
+    # host launch overhead between the step's kernels (the library enqueues
+    # kernels only, so a step can be captured).
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        cg_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg_, stream=side):
+            if args.lazy_decay:
+                d3.step_lazy(cgroups, hp, scales, ws, sel_idx_out=sel)   # on the capturing stream
+            else:
+                d3.step(cgroups, hp, ws, sel_idx_out=sel)
+        for _ in range(args.warmup):
+            cg_.replay()
+        barrier()
+        torch.cuda.synchronize(device)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            cg_.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+        d3.device_status(stream)
+        gms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, device)
+        graph = {"value": job_tflops(flops_rank, world, gms), "unit": "TFLOP/s", "ms_per_step": gms,
+                 "method": "one step captured in a CUDA graph, replayed per timed step"}
+        del cg_
+
     # End to end: every step copies its gradients from pinned host memory and
     # reads the selected rows back, through the public API.  The CPU-GPU link
     # (about 210 GB/s measured on this machine) is the bound, so the copies are
@@ -469,6 +500,8 @@ def run_ours(args, rank, world, device_index):
         line["e2e"] = e2e
     if per_model is not None:
         line["per_model"] = per_model
+    if graph is not None:
+        line["graph"] = graph
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(state, groups, args.f, hp, flops_rank)
     return line
@@ -666,6 +699,8 @@ def main():
     ap.add_argument("--e2e-chunk", type=int, default=16,
                     help="matrices per pipelined sub-batch in the end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay measurement")
     ap.add_argument("--no-per-model", action="store_true",
                     help="skip the per-model table (7B at f = 1/8, 1B at f = 1, 1/2, 1/4)")
     ap.add_argument("--per-model-steps", type=int, default=10,

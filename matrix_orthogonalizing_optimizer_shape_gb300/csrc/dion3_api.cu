@@ -24,6 +24,14 @@ namespace dion3 {
 
 __device__ unsigned g_device_status = 0u;
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("DION3_PDL");
+    return v == nullptr || atoi(v) != 0;
+  }();
+  return on;
+}
+
 unsigned* device_status_ptr() {
   static std::mutex mu;
   static std::vector<unsigned*> cache;

@@ -171,15 +171,6 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0u;
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Paired-SM variant: the box lands in this CTA's shared memory and the
 // completed bytes are reported to an mbarrier that may live in the peer CTA
 // (`bar` is a shared::cluster address).
@@ -364,10 +355,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     const __half2 t = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&t);
   }
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Super-tile u of one matrix -> (super-row P, column tile bc); the CTA of
@@ -562,6 +549,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kStagingBytes + Smem::kBarBytes);
 
+  // The next kernel on the stream may be scheduled once every CTA of this one
+  // has started (programmatic dependent launch).
+  pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nkb = (p.K + BK - 1) / BK;
   const uint32_t rank = cluster_ctarank();
@@ -588,6 +578,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up done (barriers, tensor memory): wait for the previous kernel on the
+  // stream before touching global memory.
+  pdl_wait();
 
   if (warp == 0) {
     {
@@ -959,8 +952,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;
-  kern<<<grid, kThreads, Smem::kDyn, s>>>(ta, tb, tat, tbt, to, tt, p);
-  return cudaGetLastError();
+  return launch_kernel(pdl_enabled(), kern, dim3(grid), dim3(kThreads), Smem::kDyn, s, ta, tb, tat, tbt, to, tt, p);
 }
 
 }  // namespace dion3

@@ -8,6 +8,43 @@
 
 namespace dion3 {
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The tensor-core GEMMs are launched with
+// programmatic stream serialization: their CTAs may be scheduled while the
+// previous kernel on the stream is finishing, run their set-up (barriers,
+// tensor memory), and then wait in pdl_wait() until that kernel has completed
+// and its memory is visible; no global memory is touched before the wait.
+// Every kernel calls pdl_trigger() first, so a following GEMM may be scheduled
+// as soon as all of its CTAs have started.  The memory-bound kernels are
+// launched without the attribute (their early CTAs would sit beside a running
+// GEMM: measured slower), so for them both instructions do nothing.
+// DION3_PDL=0 turns the attribute off everywhere.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether GEMM launches carry the attribute (DION3_PDL, read once; default on).
+bool pdl_enabled();
+
+// Launch with or without the programmatic-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (pdl) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Device status word bits (written by bounded device-side waits and checks).
 enum : unsigned { kDevTimeout = 1u, kDevCheck = 2u };
 

@@ -63,6 +63,8 @@ __device__ __forceinline__ float load_grad(const void* g, size_t i, int gd) {
 // ---------------------------------------------------------------------------
 template <bool VEC, int GD>  // GD: kF32, kBF16, or -1 (no gradient: norms only)
 __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constant__ AccumArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
   const long long total = static_cast<long long>(a.batch) * a.rows;
@@ -181,6 +183,8 @@ __device__ __forceinline__ int block_excl_scan_flag(bool flag, int* warp_tot, in
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ unsigned hist[256];
   __shared__ unsigned s_prefix;
   __shared__ int s_need;
@@ -265,6 +269,8 @@ constexpr int kGRows = 32, kGCols = 128;
 
 template <bool SRC_F32, bool VEC, bool BF16>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherArgs a) {
+  pdl_trigger();
+  pdl_wait();
   // Column-major staging: a pitch of 34 halves (17 words) spreads the 2-byte
   // writes of a warp over 8 banks (4-way conflicts; a 16-byte-aligned pitch of
   // 40 gave 16-way conflicts and cost a quarter of the kernel's time).
@@ -376,6 +382,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 // chunk of matrix b.
 template <bool BF16>
 __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long long n, float* parts, int nparts) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[8];
   const int b = blockIdx.y, p = blockIdx.x;
   const long long chunk = ((n + nparts - 1) / nparts + 7) / 8 * 8;
@@ -416,6 +424,8 @@ __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long lo
 // ---------------------------------------------------------------------------
 template <int PD, bool VEC, bool BF16>
 __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ ScatterArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
   const long long total = static_cast<long long>(a.batch) * a.k;
@@ -477,6 +487,8 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
 // M[b][r] <- fp32(s M[b][r]) for rows whose pending factor s is not 1; s <- 1.
 // One warp per row; rows with s = 1 cost one load.
 __global__ void __launch_bounds__(256) flush_scale_kernel(const __grid_constant__ FlushArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
   if (gw >= static_cast<long long>(a.batch) * a.rows) return;
@@ -495,81 +507,56 @@ inline unsigned ceil_div(long long a, long long b) { return static_cast<unsigned
 
 cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.rows;
-  const dim3 grid(ceil_div(total, 8)), block(256);
   const bool has_grad = a.G[0] != nullptr;
-  if (vec) {
-    if (!has_grad) accum_rownorm_kernel<true, -1><<<grid, block, 0, s>>>(a);
-    else if (a.grad_dtype == kBF16) accum_rownorm_kernel<true, kBF16><<<grid, block, 0, s>>>(a);
-    else accum_rownorm_kernel<true, kF32><<<grid, block, 0, s>>>(a);
-  } else {
-    if (!has_grad) accum_rownorm_kernel<false, -1><<<grid, block, 0, s>>>(a);
-    else if (a.grad_dtype == kBF16) accum_rownorm_kernel<false, kBF16><<<grid, block, 0, s>>>(a);
-    else accum_rownorm_kernel<false, kF32><<<grid, block, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  void (*k)(AccumArgs);
+  if (vec)
+    k = !has_grad ? accum_rownorm_kernel<true, -1>
+                  : (a.grad_dtype == kBF16 ? accum_rownorm_kernel<true, kBF16> : accum_rownorm_kernel<true, kF32>);
+  else
+    k = !has_grad ? accum_rownorm_kernel<false, -1>
+                  : (a.grad_dtype == kBF16 ? accum_rownorm_kernel<false, kBF16> : accum_rownorm_kernel<false, kF32>);
+  return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_flush_scale(const FlushArgs& a, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.rows;
-  flush_scale_kernel<<<ceil_div(total, 8), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(false, flush_scale_kernel, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
-  topk_kernel<<<a.batch, kTopkThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(false, topk_kernel, dim3(a.batch), dim3(kTopkThreads), 0, s, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
   const dim3 grid(ceil_div(a.m, kGCols), ceil_div(a.k, kGRows), a.batch), block(256);
+  void (*k)(GatherArgs);
   if (a.bf16) {
-    if (a.src_f32) {
-      if (vec) gather_kernel<true, true, true><<<grid, block, 0, s>>>(a);
-      else gather_kernel<true, false, true><<<grid, block, 0, s>>>(a);
-    } else {
-      if (vec) gather_kernel<false, true, true><<<grid, block, 0, s>>>(a);
-      else gather_kernel<false, false, true><<<grid, block, 0, s>>>(a);
-    }
+    if (a.src_f32) k = vec ? gather_kernel<true, true, true> : gather_kernel<true, false, true>;
+    else k = vec ? gather_kernel<false, true, true> : gather_kernel<false, false, true>;
   } else {
-    if (a.src_f32) {
-      if (vec) gather_kernel<true, true, false><<<grid, block, 0, s>>>(a);
-      else gather_kernel<true, false, false><<<grid, block, 0, s>>>(a);
-    } else {
-      if (vec) gather_kernel<false, true, false><<<grid, block, 0, s>>>(a);
-      else gather_kernel<false, false, false><<<grid, block, 0, s>>>(a);
-    }
+    if (a.src_f32) k = vec ? gather_kernel<true, true, false> : gather_kernel<true, false, false>;
+    else k = vec ? gather_kernel<false, true, false> : gather_kernel<false, false, false>;
   }
-  return cudaGetLastError();
+  return launch_kernel(false, k, grid, block, 0, s, a);
 }
 
 cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* parts, int nparts, bool bf16,
                              cudaStream_t s) {
-  if (bf16) sumsq_f16_kernel<true><<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
-  else sumsq_f16_kernel<false><<<dim3(nparts, batch), 256, 0, s>>>(X, n, parts, nparts);
-  return cudaGetLastError();
+  return launch_kernel(false, bf16 ? sumsq_f16_kernel<true> : sumsq_f16_kernel<false>, dim3(nparts, batch), dim3(256), 0,
+                       s, X, n, parts, nparts);
 }
 
 cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.k;
-  const dim3 grid(ceil_div(total, 8)), block(256);
+  void (*k)(ScatterArgs);
   if (a.param_dtype == kBF16) {
-    if (a.o_bf16) {
-      if (vec) scatter_kernel<kBF16, true, true><<<grid, block, 0, s>>>(a);
-      else scatter_kernel<kBF16, false, true><<<grid, block, 0, s>>>(a);
-    } else {
-      if (vec) scatter_kernel<kBF16, true, false><<<grid, block, 0, s>>>(a);
-      else scatter_kernel<kBF16, false, false><<<grid, block, 0, s>>>(a);
-    }
+    if (a.o_bf16) k = vec ? scatter_kernel<kBF16, true, true> : scatter_kernel<kBF16, false, true>;
+    else k = vec ? scatter_kernel<kBF16, true, false> : scatter_kernel<kBF16, false, false>;
   } else {
-    if (a.o_bf16) {
-      if (vec) scatter_kernel<kF32, true, true><<<grid, block, 0, s>>>(a);
-      else scatter_kernel<kF32, false, true><<<grid, block, 0, s>>>(a);
-    } else {
-      if (vec) scatter_kernel<kF32, true, false><<<grid, block, 0, s>>>(a);
-      else scatter_kernel<kF32, false, false><<<grid, block, 0, s>>>(a);
-    }
+    if (a.o_bf16) k = vec ? scatter_kernel<kF32, true, true> : scatter_kernel<kF32, false, true>;
+    else k = vec ? scatter_kernel<kF32, true, false> : scatter_kernel<kF32, false, false>;
   }
-  return cudaGetLastError();
+  return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
 }
 
 }  // namespace dion3
