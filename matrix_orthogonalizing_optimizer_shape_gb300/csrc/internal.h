@@ -82,8 +82,10 @@ struct TopkArgs {
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
-// a2: gather + normalise (+ optional decay of the source rows) into fp16, in
-// both orientations: rows-major [k][ld_rows] and columns-major [m][ld_cols].
+// a2: gather + normalise (+ optional decay of the source rows) into fp16,
+// rows-major [k][ld_rows] and, if out_cols is set, also columns-major
+// [m][ld_cols] (the standard-NS comparison path; the Gram path reads the
+// other orientation through transposed GEMM operands).
 struct GatherArgs {
   int n;                           // rows of each source matrix (bounds check of idx)
   int k, m, batch;                 // batch <= kMaxBatchPerLaunch when src_f32
@@ -138,6 +140,7 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s);
 enum GemmMode : int {
   kRect = 0,      // every tile; write `out` (normal) and/or `outT` (transposed)
   kSymLower = 1,  // M == N, lower-triangle tiles only; `out` gets the tile and its mirror
+                  // (with out_half, the mirror on the diagonal super-tiles only)
 };
 
 struct GemmDesc {
