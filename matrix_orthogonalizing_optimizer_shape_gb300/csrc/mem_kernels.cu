@@ -378,6 +378,82 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
   }
 }
 
+// a2, rows orientation only (the Gram path): one warp per selected row, 8
+// elements per lane per step, so each warp streams whole rows (the tiled
+// kernel above reads 512-byte row pieces).  Same arithmetic as the tiled
+// kernel: inv = 1 / (sqrt(sum of the fro2 parts) + eps), X = e16(v * inv), and
+// the decay mu v written back in fp32.
+template <bool SRC_F32, bool VEC, bool BF16>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant__ GatherArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  if (gw >= total) return;
+  const int b = static_cast<int>(gw / a.k);
+  const int i = static_cast<int>(gw % a.k);
+  float f2 = 0.f;
+  for (int p = 0; p < a.fro2_parts; ++p) f2 += a.fro2[static_cast<size_t>(b) * a.fro2_parts + p];
+  const float inv = 1.0f / (sqrtf(f2) + a.eps);
+  __half* dst = a.out_rows + static_cast<long long>(b) * a.rows_bstride + static_cast<size_t>(i) * a.ld_rows;
+  const int m = a.m;
+  if constexpr (SRC_F32) {
+    const int row = a.idx[static_cast<size_t>(b) * a.k + i];
+    if (row < 0 || row >= a.n) {  // never expected: record it and skip the access
+      if (lane == 0) atomicOr(a.status, kDevCheck);
+      return;
+    }
+    if (a.scale_out != nullptr && lane == 0) a.scale_out[static_cast<size_t>(b) * a.n + row] = a.mu;
+    float* src = a.M[b] + static_cast<size_t>(row) * m;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < m; c += kWarp * 8) {
+        const float4 x0 = *reinterpret_cast<const float4*>(src + c);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + c + 4);
+        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __half2 q = __halves2half2(f32_to_e16<BF16>(v[2 * j] * inv), f32_to_e16<BF16>(v[2 * j + 1] * inv));
+          w[j] = *reinterpret_cast<uint32_t*>(&q);
+        }
+        *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (a.decay) {
+          *reinterpret_cast<float4*>(src + c) =
+              make_float4(__fmul_rn(a.mu, x0.x), __fmul_rn(a.mu, x0.y), __fmul_rn(a.mu, x0.z), __fmul_rn(a.mu, x0.w));
+          *reinterpret_cast<float4*>(src + c + 4) =
+              make_float4(__fmul_rn(a.mu, x1.x), __fmul_rn(a.mu, x1.y), __fmul_rn(a.mu, x1.z), __fmul_rn(a.mu, x1.w));
+        }
+      }
+    } else {
+      for (int c = lane; c < m; c += kWarp) {
+        const float v = src[c];
+        dst[c] = f32_to_e16<BF16>(v * inv);
+        if (a.decay) src[c] = __fmul_rn(a.mu, v);
+      }
+    }
+  } else {
+    const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * m;
+    if constexpr (VEC) {
+      for (int c = lane * 8; c < m; c += kWarp * 8) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src + c);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = e16x2_to_f32<BF16>(xw[j]);
+          __half2 q = __halves2half2(f32_to_e16<BF16>(f.x * inv), f32_to_e16<BF16>(f.y * inv));
+          w[j] = *reinterpret_cast<uint32_t*>(&q);
+        }
+        *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      for (int c = lane; c < m; c += kWarp)
+        dst[c] = f32_to_e16<BF16>(e16_to_f32<BF16>(__half_as_ushort(src[c])) * inv);
+    }
+  }
+}
+
 // Sum of squares of fp16 X: grid (nparts, batch); part p covers a contiguous
 // chunk of matrix b.
 template <bool BF16>
@@ -528,6 +604,21 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
+  if (a.out_cols == nullptr) {
+    // Rows only: whole-row warps; 16-byte accesses need m and the pitch in
+    // multiples of 8 (and 16-byte aligned bases, which the callers keep).
+    const bool v8 = vec && a.m % 8 == 0 && a.ld_rows % 8 == 0;
+    void (*k)(GatherArgs);
+    if (a.bf16) {
+      if (a.src_f32) k = v8 ? gather_rows_kernel<true, true, true> : gather_rows_kernel<true, false, true>;
+      else k = v8 ? gather_rows_kernel<false, true, true> : gather_rows_kernel<false, false, true>;
+    } else {
+      if (a.src_f32) k = v8 ? gather_rows_kernel<true, true, false> : gather_rows_kernel<true, false, false>;
+      else k = v8 ? gather_rows_kernel<false, true, false> : gather_rows_kernel<false, false, false>;
+    }
+    const long long total = static_cast<long long>(a.batch) * a.k;
+    return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+  }
   const dim3 grid(ceil_div(a.m, kGCols), ceil_div(a.k, kGRows), a.batch), block(256);
   void (*k)(GatherArgs);
   if (a.bf16) {
