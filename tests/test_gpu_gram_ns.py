@@ -29,7 +29,7 @@ def _inputs(batch, k, m, seed):
 
 
 @pytest.mark.parametrize("k,m", [(64, 256), (256, 64), (128, 128), (200, 520), (520, 200),
-                                 (256, 1024), (1000, 300), (8, 72)])
+                                 (256, 1024), (1000, 300), (8, 72), (100, 250), (333, 90)])
 @pytest.mark.parametrize("restart", [3, 0])
 def test_gram_ns_matches_oracle(cuda_lib, k, m, restart):
     X = _inputs(2, k, m, seed=k * 7 + m)
