@@ -378,11 +378,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
   }
 }
 
-// a2, rows orientation only (the Gram path): one warp per selected row, 8
-// elements per lane per step, so each warp streams whole rows (the tiled
-// kernel above reads 512-byte row pieces).  Same arithmetic as the tiled
+// a2, rows orientation only (the Gram path): one warp per selected row and
+// column span of kGSpan (grid.y), 8 elements per lane per step, so each warp
+// streams 8 KB row pieces (the tiled kernel above reads 512-byte pieces).  Same arithmetic as the tiled
 // kernel: inv = 1 / (sqrt(sum of the fro2 parts) + eps), X = e16(v * inv), and
 // the decay mu v written back in fp32.
+constexpr int kGSpan = 2048;
+
 template <bool SRC_F32, bool VEC, bool BF16>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant__ GatherArgs a) {
   pdl_trigger();
@@ -397,45 +399,62 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
   for (int p = 0; p < a.fro2_parts; ++p) f2 += a.fro2[static_cast<size_t>(b) * a.fro2_parts + p];
   const float inv = 1.0f / (sqrtf(f2) + a.eps);
   __half* dst = a.out_rows + static_cast<long long>(b) * a.rows_bstride + static_cast<size_t>(i) * a.ld_rows;
-  const int m = a.m;
+  const int cbeg = blockIdx.y * kGSpan;
+  const int m = a.m - cbeg < kGSpan ? a.m : cbeg + kGSpan;  // end of this warp's columns
   if constexpr (SRC_F32) {
     const int row = a.idx[static_cast<size_t>(b) * a.k + i];
     if (row < 0 || row >= a.n) {  // never expected: record it and skip the access
       if (lane == 0) atomicOr(a.status, kDevCheck);
       return;
     }
-    if (a.scale_out != nullptr && lane == 0) a.scale_out[static_cast<size_t>(b) * a.n + row] = a.mu;
-    float* src = a.M[b] + static_cast<size_t>(row) * m;
+    if (a.scale_out != nullptr && lane == 0 && blockIdx.y == 0)
+      a.scale_out[static_cast<size_t>(b) * a.n + row] = a.mu;
+    float* src = a.M[b] + static_cast<size_t>(row) * a.m;
     if constexpr (VEC) {
-      for (int c = lane * 8; c < m; c += kWarp * 8) {
-        const float4 x0 = *reinterpret_cast<const float4*>(src + c);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + c + 4);
-        const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        uint32_t w[4];
+      constexpr int U = 2;  // steps of loads in flight per lane
+      const int step = kWarp * 8;
+      for (int c0 = cbeg + lane * 8; c0 < m; c0 += step * U) {
+        float4 x[U][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          __half2 q = __halves2half2(f32_to_e16<BF16>(v[2 * j] * inv), f32_to_e16<BF16>(v[2 * j + 1] * inv));
-          w[j] = *reinterpret_cast<uint32_t*>(&q);
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + u * step;
+          if (c < m) {
+            x[u][0] = *reinterpret_cast<const float4*>(src + c);
+            x[u][1] = *reinterpret_cast<const float4*>(src + c + 4);
+          }
         }
-        *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
-        if (a.decay) {
-          *reinterpret_cast<float4*>(src + c) =
-              make_float4(__fmul_rn(a.mu, x0.x), __fmul_rn(a.mu, x0.y), __fmul_rn(a.mu, x0.z), __fmul_rn(a.mu, x0.w));
-          *reinterpret_cast<float4*>(src + c + 4) =
-              make_float4(__fmul_rn(a.mu, x1.x), __fmul_rn(a.mu, x1.y), __fmul_rn(a.mu, x1.z), __fmul_rn(a.mu, x1.w));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + u * step;
+          if (c >= m) continue;
+          const float4 x0 = x[u][0], x1 = x[u][1];
+          const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __half2 q = __halves2half2(f32_to_e16<BF16>(v[2 * j] * inv), f32_to_e16<BF16>(v[2 * j + 1] * inv));
+            w[j] = *reinterpret_cast<uint32_t*>(&q);
+          }
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (a.decay) {
+            *reinterpret_cast<float4*>(src + c) =
+                make_float4(__fmul_rn(a.mu, x0.x), __fmul_rn(a.mu, x0.y), __fmul_rn(a.mu, x0.z), __fmul_rn(a.mu, x0.w));
+            *reinterpret_cast<float4*>(src + c + 4) =
+                make_float4(__fmul_rn(a.mu, x1.x), __fmul_rn(a.mu, x1.y), __fmul_rn(a.mu, x1.z), __fmul_rn(a.mu, x1.w));
+          }
         }
       }
     } else {
-      for (int c = lane; c < m; c += kWarp) {
+      for (int c = cbeg + lane; c < m; c += kWarp) {
         const float v = src[c];
         dst[c] = f32_to_e16<BF16>(v * inv);
         if (a.decay) src[c] = __fmul_rn(a.mu, v);
       }
     }
   } else {
-    const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * m;
+    const __half* src = a.X + (static_cast<size_t>(b) * a.k + i) * a.m;
     if constexpr (VEC) {
-      for (int c = lane * 8; c < m; c += kWarp * 8) {
+      for (int c = cbeg + lane * 8; c < m; c += kWarp * 8) {
         const uint4 x = *reinterpret_cast<const uint4*>(src + c);
         const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
         uint32_t w[4];
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
         *reinterpret_cast<uint4*>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
-      for (int c = lane; c < m; c += kWarp)
+      for (int c = cbeg + lane; c < m; c += kWarp)
         dst[c] = f32_to_e16<BF16>(e16_to_f32<BF16>(__half_as_ushort(src[c])) * inv);
     }
   }
@@ -617,7 +636,7 @@ cudaError_t launch_gather(const GatherArgs& a, bool vec, cudaStream_t s) {
       else k = v8 ? gather_rows_kernel<false, true, false> : gather_rows_kernel<false, false, false>;
     }
     const long long total = static_cast<long long>(a.batch) * a.k;
-    return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+    return launch_kernel(false, k, dim3(ceil_div(total, 8), ceil_div(a.m, kGSpan)), dim3(256), 0, s, a);
   }
   const dim3 grid(ceil_div(a.m, kGCols), ceil_div(a.k, kGRows), a.batch), block(256);
   void (*k)(GatherArgs);
