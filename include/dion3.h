@@ -23,7 +23,13 @@
  *     pointer must be 16-byte aligned; the workspace 256-byte aligned.
  *   - Ordering: every call only enqueues work on `stream` and returns without
  *     synchronising; results are visible to later work on the same stream.
- *     Calls that share one workspace must not overlap on the device.
+ *     Calls that share one workspace must not overlap on the device.  Since a
+ *     call enqueues kernel launches only (no host synchronisation, no
+ *     allocation), it can be captured in a CUDA graph and replayed.  The
+ *     tensor-core kernels are launched with programmatic dependent launch
+ *     (their set-up may overlap the end of the previous kernel on the stream;
+ *     they read nothing before it has completed); the environment variable
+ *     DION3_PDL=0 turns that off.
  *   - Errors: arguments are validated on the host before the first launch; an
  *     invalid call returns a status != DION3_OK, enqueues nothing and leaves
  *     every tensor untouched.  A failed launch returns DION3_ERR_CUDA.
