@@ -76,13 +76,14 @@ def _check_set(name, f, seed):
     return near
 
 
-@pytest.mark.parametrize("f", [0.25, 1.0])
+@pytest.mark.parametrize("f", [0.25, 0.5, 1.0])
 def test_full_1b_set(cuda_lib, f):
     _check_set("1b", f, seed=11)
 
 
-def test_full_7b_set_quarter(cuda_lib):
-    _check_set("7b", 0.25, seed=12)
+@pytest.mark.parametrize("f", [0.25, 0.125])
+def test_full_7b_set(cuda_lib, f):
+    _check_set("7b", f, seed=12)
     torch.cuda.empty_cache()
 
 
