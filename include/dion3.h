@@ -272,7 +272,15 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups,
  *   sel_idx_out  NULL, or a host array [ngroups] of device int32 [batch][k]
  *                buffers (entries may be NULL) that receive each matrix's
  *                selected rows, ascending.
- * Groups are processed in order on `stream`.
+ * With more than one group, the groups run concurrently: each on one of up to
+ * four streams owned by the library, forked from `stream` (they wait for the
+ * work already enqueued on it) and joined back into it before the call
+ * returns, so later work on `stream` sees every result, and a graph captured
+ * on `stream` holds the forked branches.  No matrix may belong to two groups
+ * of one call.  While the launch trace is enabled, or when the environment
+ * variable DION3_GROUP_STREAMS=0 is set, the groups run in order on `stream`.
+ * The library's streams are created the first time a device needs them, so
+ * make the first multi-group call before any stream capture begins.
  */
 dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
                         const dion3_hparams* hp, void* ws, size_t ws_bytes,

@@ -804,6 +804,78 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups, co
 }  // extern "C"
 
 namespace {
+// Streams (one per group, up to kGroupStreams, reused round-robin) and events
+// for running the shape groups of one step concurrently.  The per-device pool
+// is created on first use; a call holds the pool's lock from the fork to the
+// join, so the events are never re-recorded by another host thread in
+// between.  DION3_GROUP_STREAMS=0 runs every group on the caller's stream, and
+// so does the launch trace, whose per-launch events would otherwise time
+// overlapping kernels.
+constexpr int kGroupStreams = 4;
+struct StreamPool {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t streams[kGroupStreams] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t done[kGroupStreams] = {};
+};
+StreamPool g_pools[64];
+
+bool group_streams_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("DION3_GROUP_STREAMS");
+    return v == nullptr || atoi(v) != 0;
+  }();
+  if (!on) return false;
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  return !g_trace_on;
+}
+
+class GroupStreams {
+ public:
+  cudaError_t begin(cudaStream_t caller, int ngroups) {
+    caller_ = caller;
+    n_ = (ngroups > 1 && group_streams_enabled()) ? std::min(ngroups, kGroupStreams) : 0;
+    if (n_ == 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    pool_ = &g_pools[dev & 63];
+    lock_ = std::unique_lock<std::mutex>(pool_->mu);
+    if (!pool_->ready) {
+      for (int i = 0; i < kGroupStreams; ++i) {
+        if ((e = cudaStreamCreateWithFlags(&pool_->streams[i], cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&pool_->done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      }
+      if ((e = cudaEventCreateWithFlags(&pool_->fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+      pool_->ready = true;
+    }
+    if ((e = cudaEventRecord(pool_->fork, caller_)) != cudaSuccess) return e;
+    for (int i = 0; i < n_; ++i)
+      if ((e = cudaStreamWaitEvent(pool_->streams[i], pool_->fork, 0)) != cudaSuccess) return e;
+    return cudaSuccess;
+  }
+  cudaStream_t stream(int gi) const { return n_ == 0 ? caller_ : pool_->streams[gi % n_]; }
+  cudaError_t end() {
+    if (n_ == 0) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_ && e == cudaSuccess; ++i) {
+      e = cudaEventRecord(pool_->done[i], pool_->streams[i]);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(caller_, pool_->done[i], 0);
+    }
+    n_ = 0;
+    if (lock_.owns_lock()) lock_.unlock();
+    return e;
+  }
+  ~GroupStreams() { end(); }
+
+ private:
+  cudaStream_t caller_ = nullptr;
+  int n_ = 0;
+  StreamPool* pool_ = nullptr;
+  std::unique_lock<std::mutex> lock_;
+};
+
 // The step of dion3_step; with row_scale (one [batch][rows] fp32 buffer per
 // group) the decay of the selected momentum rows is left pending in row_scale
 // instead of being written back (dion3_step_lazy).
@@ -828,13 +900,23 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
   unsigned* st = device_status_ptr();
   if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream);
   const float lr_eff = static_cast<float>(static_cast<double>(hp->lr) / std::sqrt(static_cast<double>(hp->f)));
-  Carver c{static_cast<char*>(ws)};
+  // Every group has its own part of the workspace, so the groups are
+  // independent: with more than one, each runs on a stream of its own, forked
+  // from and joined back into the caller's stream (capturable in a graph).
+  std::vector<GroupPlan> plans(ngroups);
+  {
+    Carver c{static_cast<char*>(ws)};
+    for (int gi = 0; gi < ngroups; ++gi) plan_group(c, groups[gi], hp->f, plans[gi]);
+  }
+  GroupStreams fork;
+  cudaError_t fe = fork.begin(s0, ngroups);
+  if (fe != cudaSuccess) return cuda_fail(fe, "group stream fork");
   for (int gi = 0; gi < ngroups; ++gi) {
     const dion3_group& g = groups[gi];
-    GroupPlan gp;
-    plan_group(c, g, hp->f, gp);
+    const GroupPlan& gp = plans[gi];
+    cudaStream_t s = fork.stream(gi);
     int32_t* idx = (sel_idx_out != nullptr && sel_idx_out[gi] != nullptr) ? sel_idx_out[gi] : gp.idx;
     const bool vec = g.cols % 8 == 0;
     cudaError_t e;
@@ -869,7 +951,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       ga.n = g.rows; ga.status = st;
       gather_targets(gp.ns, ga);
       ga.out_rows += ga.rows_bstride * b0;
-      ga.out_cols += ga.cols_bstride * b0;
+      if (ga.out_cols != nullptr) ga.out_cols += ga.cols_bstride * b0;
       if ((e = traced_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
     }
     NsOut out{gp.O, gp.o_bs, gp.ld_o};
@@ -888,6 +970,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
   }
+  if ((fe = fork.end()) != cudaSuccess) return cuda_fail(fe, "group stream join");
   return ok();
 }
 }  // namespace
