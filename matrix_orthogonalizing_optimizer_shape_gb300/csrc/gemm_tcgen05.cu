@@ -20,7 +20,12 @@
 // MN-major bit of the instruction descriptor set.  Both CTAs of a pair have
 // the same 256-row super-row, so they always agree on the orientation.  This
 // skips the mirror writes outside the diagonal blocks and never touches the
-// upper triangle.  The same MN-major tiles read an operand that is given as its
+// upper triangle.  When the product is A A^T (plus beta A, with A half-stored,
+// and gamma I), a diagonal super-tile is written whole as computed instead of
+// mirrored (diag_full): element (i, j) and (j, i) are the same sum of the same
+// products in the same order, so the tile is exactly symmetric either way, and
+// every epilogue warp then writes the same number of chunks.  The same MN-major
+// tiles read an operand that is given as its
 // transpose (a_tr / b_tr: A stored [K][M]), so a matrix kept in one orientation
 // serves as A = Y or A = Y^T alike.
 //
@@ -73,6 +78,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -102,6 +108,7 @@ struct GemmParams {
   int a_half, b_half;        // A / B is a half-stored symmetric matrix (M == K / N == K)
   int a_tr, b_tr;            // A / B is given as its transpose ([K][M] / [K][N]): all tiles MN-major
   int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
+  int diag_full;             // out_half: diagonal super-tiles written whole, as computed (no mirror)
   unsigned* status;
 };
 
@@ -500,7 +507,7 @@ __device__ __forceinline__ uint16_t half_bits(const uint32_t (&hp)[16], int j) {
 __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx, int r, int c0, int row0,
                                                    const uint32_t (&hp)[16], bool mirror) {
   if (r >= p.M) return;
-  const bool sym = p.mode == kSymLower;
+  const bool sym = p.mode == kSymLower && !p.diag_full;
   const bool full = (c0 + 32 <= p.N);
   const bool below = !sym || (row0 > c0 + 31);
   __half* outb = p.out ? p.out + static_cast<long long>(bidx) * p.out_bs : nullptr;
@@ -689,7 +696,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
       // The transposed box of this tile: outT, or the mirror of a symmetric
       // result (a half-stored one is mirrored on the diagonal super-tiles only).
-      const bool want_t = sym ? (!p.out_half || P == bc) : p.outT != nullptr;
+      const bool want_t = sym ? (!p.out_half || (P == bc && !p.diag_full)) : p.outT != nullptr;
+      // Chunks above the diagonal are skipped, and chunks on it take the
+      // element-wise path, unless the diagonal super-tile is written whole.
+      const bool tri = sym && !p.diag_full;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
       // C of every chunk this warp will write (registers; unused entries stay
@@ -698,7 +708,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kChunks; ++i) {
         const int c0 = bc * BN + col_lo + 32 * i;
-        if (c0 < p.N && !(sym && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
+        if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
       if (!ok) break;
@@ -710,14 +720,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int c0 = bc * BN + cc;
         // Warp-uniform classification of the chunk.
         if (c0 >= p.N) break;
-        if (sym && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
+        if (tri && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
         if (row0 >= p.M) continue;            // rows out of range
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
         uint32_t hp[16];
         chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
-        if (!tma_ok || (sym && row0 <= c0 + 31)) {
+        if (!tma_ok || (tri && row0 <= c0 + 31)) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
           continue;
         }
@@ -824,6 +834,16 @@ bool make_map(CUtensorMap* map, const __half* ptr, long long bstride, int ld, in
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Whether self-products write their diagonal super-tiles whole
+// (DION3_DIAG_FULL, read once; default on).
+bool diag_full_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("DION3_DIAG_FULL");
+    return v == nullptr || atoi(v) != 0;
+  }();
+  return on;
 }
 
 // Clusters of this kernel that fit on the device at once (persistent grid).
@@ -948,6 +968,13 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.b_tr = g.b_tr ? 1 : 0;
   p.b_half = g.b_half ? 1 : 0;
   p.out_half = g.out_half ? 1 : 0;
+  // A A^T (+ beta C with C = A half-stored, + gamma I): exactly symmetric as
+  // computed, so the diagonal super-tiles of a half-stored result need no mirror.
+  const bool self = g.A == g.B && g.lda == g.ldb && g.a_bstride == g.b_bstride && g.a_tr == g.b_tr &&
+                    g.a_half == g.b_half;
+  const bool c_sym = g.C == nullptr || g.beta == 0.0f ||
+                     (g.a_half && g.C == g.A && g.ldc == g.lda && g.c_bstride == g.a_bstride);
+  p.diag_full = (g.mode == kSymLower && g.out_half && self && c_sym && diag_full_enabled()) ? 1 : 0;
   p.status = dev_status;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));

@@ -153,3 +153,58 @@ def test_syrk_from_transposed_storage(cuda_lib):
     got = _np(R[:, :, :s])
     assert (got[:, ~mask] == 7.0).all()
     assert rel_fro(np.where(mask, got, 0), np.where(mask, want, 0)) < 2e-3
+
+
+@pytest.mark.parametrize("s,batch", [(256, 2), (700, 2), (1024, 1)])
+@pytest.mark.parametrize("with_c", [False, True])
+def test_self_product_diagonal_blocks_whole(cuda_lib, s, batch, with_c):
+    """R R^T (+ b R + a I) with A, B and C the same half-stored matrix: the
+    diagonal blocks are written whole as computed, not mirrored.  Entry (i, j)
+    and (j, i) are the same sum of the same products, so the result equals,
+    bit for bit, the mirrored result of the same product with B (and C) in
+    another buffer holding the same values."""
+    rng = np.random.default_rng(s + batch + 100 * with_c)
+    R = _as_half_stored(_dev(_sym(rng, batch, s, 1.0 / np.sqrt(s))), s)
+    R2 = R.clone()
+    a, b, c = d3.MUON_QUINTIC
+    whole = _dev(np.full((batch, s, s), 7.0))
+    mirrored = _dev(np.full((batch, s, s), 7.0))
+    beta = b if with_c else 0.0
+    d3.gemm_f16(R[:, :, :s], R[:, :, :s], D=whole[:, :, :s], C=R[:, :, :s] if with_c else None,
+                mode=SYM_HALF, alpha=c, beta=beta, gamma=a)
+    d3.gemm_f16(R[:, :, :s], R2[:, :, :s], D=mirrored[:, :, :s], C=R2[:, :, :s] if with_c else None,
+                mode=SYM_HALF, alpha=c, beta=beta, gamma=a)
+    torch.cuda.synchronize()
+    mask = _half_mask(s)
+    got, ref = _np(whole[:, :, :s]), _np(mirrored[:, :, :s])
+    assert np.isfinite(got[:, mask]).all()
+    assert np.array_equal(got[:, mask], ref[:, mask])
+    assert (got[:, ~mask] == 7.0).all()
+    R64 = np.where(mask, _np(R[:, :, :s]), np.swapaxes(np.nan_to_num(_np(R[:, :, :s])), 1, 2))
+    want = c * R64 @ R64 + beta * R64 + a * np.eye(s)
+    assert rel_fro(np.where(mask, got, 0), np.where(mask, want, 0)) < 2e-3
+
+
+@pytest.mark.parametrize("tr", [False, True])
+def test_syrk_diagonal_blocks_whole(cuda_lib, tr):
+    """Y Y^T written half-stored from one buffer (diagonal blocks whole) equals
+    the mirrored result with B in a copy of Y, bit for bit."""
+    rng = np.random.default_rng(9 + tr)
+    batch, s, L = 2, 600, 1300
+    if tr:
+        Yf = _dev(rng.standard_normal((batch, L, s)) / np.sqrt(L))
+        Y, Y2 = Yf[:, :, :s], Yf.clone()[:, :, :s]
+        mode = d3.GEMM_SYM_LOWER | d3.GEMM_OUT_HALF | d3.GEMM_A_TRANS | d3.GEMM_B_TRANS
+    else:
+        Yf = _dev(rng.standard_normal((batch, s, L)) / np.sqrt(L))
+        Y, Y2 = Yf[:, :, :L], Yf.clone()[:, :, :L]
+        mode = d3.GEMM_SYM_LOWER | d3.GEMM_OUT_HALF
+    whole = _dev(np.full((batch, s, s), 7.0))
+    mirrored = _dev(np.full((batch, s, s), 7.0))
+    d3.gemm_f16(Y, Y, D=whole[:, :, :s], mode=mode)
+    d3.gemm_f16(Y, Y2, D=mirrored[:, :, :s], mode=mode)
+    torch.cuda.synchronize()
+    mask = _half_mask(s)
+    got, ref = _np(whole[:, :, :s]), _np(mirrored[:, :, :s])
+    assert np.array_equal(got[:, mask], ref[:, mask])
+    assert (got[:, ~mask] == 7.0).all()
