@@ -808,7 +808,7 @@ namespace {
 // for running the shape groups of one step concurrently.  The per-device pool
 // is created on first use; a call holds the pool's lock from the fork to the
 // join, so the events are never re-recorded by another host thread in
-// between.  DION3_GROUP_STREAMS=0 runs every group on the caller's stream, and
+// between.  The streams and events live until the process exits.  DION3_GROUP_STREAMS=0 runs every group on the caller's stream, and
 // so does the launch trace, whose per-launch events would otherwise time
 // overlapping kernels.
 constexpr int kGroupStreams = 4;
@@ -843,11 +843,17 @@ class GroupStreams {
     pool_ = &g_pools[dev & 63];
     lock_ = std::unique_lock<std::mutex>(pool_->mu);
     if (!pool_->ready) {
+      // Handles made by an earlier, failed attempt are kept, not made again.
       for (int i = 0; i < kGroupStreams; ++i) {
-        if ((e = cudaStreamCreateWithFlags(&pool_->streams[i], cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&pool_->done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+        if (pool_->streams[i] == nullptr &&
+            (e = cudaStreamCreateWithFlags(&pool_->streams[i], cudaStreamNonBlocking)) != cudaSuccess)
+          return e;
+        if (pool_->done[i] == nullptr &&
+            (e = cudaEventCreateWithFlags(&pool_->done[i], cudaEventDisableTiming)) != cudaSuccess)
+          return e;
       }
-      if ((e = cudaEventCreateWithFlags(&pool_->fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+      if (pool_->fork == nullptr && (e = cudaEventCreateWithFlags(&pool_->fork, cudaEventDisableTiming)) != cudaSuccess)
+        return e;
       pool_->ready = true;
     }
     if ((e = cudaEventRecord(pool_->fork, caller_)) != cudaSuccess) return e;
