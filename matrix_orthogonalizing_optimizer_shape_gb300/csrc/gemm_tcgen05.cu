@@ -209,6 +209,12 @@ __device__ __forceinline__ void fence_async_shared() {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr)
+               : "memory");
+}
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
@@ -535,6 +541,42 @@ __device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx
   }
 }
 
+// A chunk on the diagonal of a triangle-only result (its first row and column
+// coincide: both are multiples of 32) is written as one symmetric 32 x 32
+// box.  The warp stages the chunk's transpose in the second half of its
+// staging buffer, then each row keeps its own values on and below the
+// diagonal, takes the rest from the transpose, and is staged in the first
+// half, ready for one bulk store.
+__device__ __forceinline__ void diag_chunk(uint32_t buf, uint32_t sw, int lane, uint32_t staged,
+                                           uint32_t (&hp)[16]) {
+  const uint32_t tbuf = buf + Smem::kStageBoxBytes;
+  if (lane == 0 && staged >= 1) bulk_wait_read_0();
+  __syncwarp();
+  const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t t[4];
+    ld_shared_v4(tbuf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), t);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = 4 * q + e;  // columns 2m and 2m + 1 of this row
+      if (2 * m > lane)
+        hp[m] = t[e];
+      else if (2 * m == lane)
+        hp[m] = (hp[m] & 0xFFFFu) | (t[e] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1], hp[4 * q + 2],
+                 hp[4 * q + 3]);
+  fence_async_shared();
+  __syncwarp();
+}
+
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -697,8 +739,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // The transposed box of this tile: outT, or the mirror of a symmetric
       // result (a half-stored one is mirrored on the diagonal super-tiles only).
       const bool want_t = sym ? (!p.out_half || (P == bc && !p.diag_full)) : p.outT != nullptr;
-      // Chunks above the diagonal are skipped, and chunks on it take the
-      // element-wise path, unless the diagonal super-tile is written whole.
+      // Chunks above the diagonal are skipped, and chunks on it are written as
+      // symmetric boxes, unless the diagonal super-tile is written whole.
       const bool tri = sym && !p.diag_full;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
@@ -727,16 +769,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         uint32_t hp[16];
         chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
-        if (!tma_ok || (tri && row0 <= c0 + 31)) {
+        if (!tma_ok) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
+          continue;
+        }
+        const uint32_t buf = my_staging;
+        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+        if (tri && row0 <= c0 + 31) {
+          diag_chunk(buf, sw, lane, staged, hp);
+          if (lane == 0) {
+            tma_store_3d(&tmOut, buf, c0, row0, bidx);
+            bulk_commit();
+          }
+          ++staged;
           continue;
         }
         // Stage the box (and its transpose) in swizzled shared memory, then
         // one lane writes them with bulk tensor stores.
-        const uint32_t buf = my_staging;
         if (lane == 0 && staged >= 1) bulk_wait_read_0();
         __syncwarp();
-        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
         if (want_n) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
