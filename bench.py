@@ -15,8 +15,9 @@ Printed (rank 0, one JSON line):
   e2e          the same metric when every step also copies its gradients from
                pinned host memory and reads the selected row indices back.
   roofline     the dominant kernel of the timed region (CUDA events around each
-               launch, via the library's launch trace) against the measured
-               peak in MEASURED_PEAKS.json.
+               memory-bound launch and each chain of GEMM launches, via the
+               library's launch trace) against the measured peak in
+               MEASURED_PEAKS.json.
   cpu_baseline the float64 CPU oracle timed on a bounded sample (one matrix of
                each shape group) and scaled to the full set.
   graph        the same step captured once in a CUDA graph and replayed.
@@ -322,7 +323,8 @@ def run_ours(args, rank, world, device_index):
         do_step(cgroups, scales, sel, ws)
     d3.device_status(stream)
 
-    # Timed region: K steps, per-launch events through the library trace.
+    # Timed region: K steps, kernel times from the library trace (events per
+    # memory-bound launch and per chain of GEMM launches).
     clocks = ClockSampler(device_index)
     barrier()
     torch.cuda.synchronize(device)

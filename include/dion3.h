@@ -310,15 +310,21 @@ dion3_status dion3_select_rows_noalloc(int32_t rows, int32_t cols, int32_t batch
                                        float* fro2_out, dion3_stream_t stream);
 
 /*
- * Launch trace (measurement aid).  While enabled, every kernel launch made by
- * this library is bracketed by two CUDA events on its stream and recorded with
- * its algorithmic work: useful FLOPs for the tensor-core GEMM (a triangle
- * counted as half) and bytes that must cross HBM for the memory-bound
- * kernels.  dion3_trace_enable(1) starts a fresh record, dion3_trace_enable(0)
- * stops and discards it.  dion3_trace_collect() waits for the recorded events,
- * aggregates them per kernel into out[0 .. min(*count, capacity)), sets *count
- * to the number of kernels seen and clears the record (recording goes on if
- * enabled).  Host-side cost: two cudaEventRecord calls per launch.
+ * Launch trace (measurement aid).  While enabled, every launch of a
+ * memory-bound kernel made by this library, and every chain of tensor-core GEMM
+ * launches of one Newton-Schulz run, is bracketed by two CUDA events on its
+ * stream and recorded with its algorithmic work: useful FLOPs for the GEMM (a
+ * triangle counted as half) and bytes that must cross HBM for the memory-bound
+ * kernels.  A chain gets one pair of events so that nothing sits between its
+ * GEMMs (each may overlap its set-up with the end of the previous one); with
+ * the environment variable DION3_TRACE_DETAIL=1 (or 2) every GEMM launch gets
+ * its own pair and is labelled by role (and Gram side).  dion3_trace_enable(1)
+ * starts a fresh record, dion3_trace_enable(0) stops and discards it.
+ * dion3_trace_collect() waits for the recorded events, aggregates them per
+ * kernel into out[0 .. min(*count, capacity)) (launches counts the launches,
+ * total_ms the time between each pair of events), sets *count to the number of
+ * kernels seen and clears the record (recording goes on if enabled).  Host-side
+ * cost: two cudaEventRecord calls per recorded pair.
  */
 typedef struct {
   char name[32];

@@ -68,14 +68,20 @@ dion3_status ok() {
 }
 
 // ---------------------------------------------------------------------------
-// Optional launch trace: when enabled, every kernel launch is bracketed by two
-// CUDA events on its stream and recorded with its algorithmic work (useful
-// FLOPs for the GEMM, bytes for the memory-bound kernels).
+// Optional launch trace: when enabled, every launch of a memory-bound kernel,
+// and every chain of GEMM launches of one Newton-Schulz run, is bracketed by
+// two CUDA events on its stream and recorded with its algorithmic work (useful
+// FLOPs for the GEMM, bytes for the memory-bound kernels) and launch count.
+// Events between the GEMMs of a chain would keep each GEMM from overlapping
+// its set-up with the end of the previous one (programmatic dependent
+// launch), so a chain gets one pair; DION3_TRACE_DETAIL=1|2 records every
+// GEMM launch on its own instead, labelled by role.
 // ---------------------------------------------------------------------------
 struct TraceRec {
   std::string name;
   cudaEvent_t a, b;
   double flops, bytes;
+  int launches;
 };
 std::mutex g_trace_mu;
 bool g_trace_on = false;
@@ -101,10 +107,70 @@ void trace_clear_locked() {
   g_trace.clear();
 }
 
+int trace_detail() {
+  static const int detail = [] {
+    const char* v = getenv("DION3_TRACE_DETAIL");
+    return v != nullptr ? atoi(v) : 0;
+  }();
+  return detail;
+}
+
+// The open chain of this host thread (launches of kernel `name` on stream s).
+struct TraceSpan {
+  std::string name;
+  cudaStream_t s = nullptr;
+  cudaEvent_t a = nullptr;
+  double flops = 0.0, bytes = 0.0;
+  int launches = 0;
+};
+thread_local TraceSpan* t_span = nullptr;
+
+// Opens a chain for the launches of `name` on `s` made while it lives (if the
+// trace is on, per-launch detail is off and no chain is open yet).
+class TraceChain {
+ public:
+  TraceChain(const char* name, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    if (!g_trace_on || trace_detail() > 0 || t_span != nullptr) return;
+    span_.name = name;
+    span_.s = s;
+    span_.a = pooled_event();
+    if (span_.a == nullptr) return;
+    cudaEventRecord(span_.a, s);
+    open_ = true;
+    t_span = &span_;
+  }
+  ~TraceChain() {
+    if (!open_) return;
+    t_span = nullptr;
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    cudaEvent_t b = (g_trace_on && span_.launches > 0) ? pooled_event() : nullptr;
+    if (b == nullptr) {
+      g_event_pool.push_back(span_.a);
+      return;
+    }
+    cudaEventRecord(b, span_.s);
+    g_trace.push_back({span_.name, span_.a, b, span_.flops, span_.bytes, span_.launches});
+  }
+  TraceChain(const TraceChain&) = delete;
+  TraceChain& operator=(const TraceChain&) = delete;
+
+ private:
+  TraceSpan span_;
+  bool open_ = false;
+};
+
 template <class Launch>
 cudaError_t traced(const std::string& name, double flops, double bytes, cudaStream_t s, Launch&& launch) {
   std::unique_lock<std::mutex> lock(g_trace_mu);
   if (!g_trace_on) {
+    lock.unlock();
+    return launch();
+  }
+  if (t_span != nullptr && t_span->name == name && t_span->s == s) {
+    t_span->flops += flops;
+    t_span->bytes += bytes;
+    ++t_span->launches;
     lock.unlock();
     return launch();
   }
@@ -113,7 +179,7 @@ cudaError_t traced(const std::string& name, double flops, double bytes, cudaStre
   cudaEventRecord(a, s);
   const cudaError_t e = launch();
   cudaEventRecord(b, s);
-  g_trace.push_back({name, a, b, flops, bytes});
+  g_trace.push_back({name, a, b, flops, bytes, 1});
   return e;
 }
 
@@ -219,10 +285,7 @@ cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
   const double flops = g.mode == kSymLower ? static_cast<double>(g.M) * g.M * g.K * g.batch
                                            : 2.0 * g.M * g.N * g.K * g.batch;
   const double bytes = 2.0 * g.batch * (static_cast<double>(g.M) * g.K + static_cast<double>(g.N) * g.K);
-  static const int detail = [] {
-    const char* v = getenv("DION3_TRACE_DETAIL");
-    return v != nullptr ? atoi(v) : 0;
-  }();
+  const int detail = trace_detail();
   std::string name = "gemm_tcgen05";
   if (detail >= 1) name = g.mode == kRect ? "gemm:rect" : (g.K == g.M ? "gemm:sym_square" : "gemm:syrk");
   if (detail >= 2) name += ":" + std::to_string(g.mode == kRect ? g.N : g.M);
@@ -290,6 +353,7 @@ struct NsOut {
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
                          cudaStream_t stream, bool dense = false) {
+  TraceChain chain("gemm_tcgen05", stream);
   // Symmetric product of two s x s matrices (or, with xi >= 0, the SYRK
   // R = Y Y^T from X[xi]: Y itself when wide, given as its transpose X = Y^T
   // otherwise).
@@ -447,6 +511,7 @@ void gather_targets_std(const StdPlan& p, GatherArgs& g) {
 
 dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
                              cudaStream_t stream, bool dense) {
+  TraceChain chain("gemm_tcgen05", stream);
   auto launch = [&](const GemmDesc& g0) -> dion3_status {
     GemmDesc g = g0;
     g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
@@ -1091,7 +1156,7 @@ dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32
       slot = &agg.back();
       snprintf(slot->name, sizeof slot->name, "%s", r.name.c_str());
     }
-    slot->launches += 1;
+    slot->launches += r.launches;
     slot->total_ms += ms;
     slot->useful_flops += r.flops;
     slot->algo_bytes += r.bytes;

@@ -88,3 +88,35 @@ def test_concurrent_groups_match_in_order(cuda_lib):
         assert np.array_equal(conc[3][gi].cpu().numpy(), seq[3][gi].cpu().numpy())
         for a, b in zip(conc[1][gi] + conc[2][gi], seq[1][gi] + seq[2][gi]):
             assert np.array_equal(to_host(a), to_host(b))
+
+
+def test_trace_counts_launches_and_work(cuda_lib):
+    """The launch trace over one step: each Newton-Schulz run's 18 GEMMs
+    (T = 5, restart before iteration 3) are timed as one chain but counted as
+    18 launches, with the useful FLOPs 6 s^2 L + 14 s^3 per matrix; every
+    memory-bound kernel launches once per group."""
+    f = 0.25
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+    groups, _, _, sels = _build(f, seed=31)
+    ws = d3.alloc_workspace(d3.workspace_size(groups, hp))
+    d3.step(groups, hp, ws, sel_idx_out=sels)
+    d3.trace_enable(True)
+    try:
+        d3.step(groups, hp, ws, sel_idx_out=sels)
+        trace = d3.trace_collect()
+    finally:
+        d3.trace_enable(False)
+    d3.device_status()
+    gemm = trace["gemm_tcgen05"]
+    assert gemm["launches"] == 18 * len(SHAPES)
+    want = 0.0
+    for n, m, batch, _ in SHAPES:
+        k = d3.num_selected(f, n)
+        s, L = min(k, m), max(k, m)
+        assert d3.useful_flops(k, m, hp) == pytest.approx(6.0 * s * s * L + 14.0 * s ** 3, rel=1e-12)
+        want += d3.useful_flops(k, m, hp) * batch
+    assert gemm["useful_flops"] == pytest.approx(want, rel=1e-9)
+    assert gemm["total_ms"] > 0
+    for name in ("accum_rownorm", "topk_select", "gather_normalize", "scatter_update"):
+        assert trace[name]["launches"] == len(SHAPES), name
+        assert trace[name]["total_ms"] > 0
