@@ -20,6 +20,10 @@ Printed (rank 0, one JSON line):
                MEASURED_PEAKS.json.
   cpu_baseline the float64 CPU oracle timed on a bounded sample (one matrix of
                each shape group) and scaled to the full set.
+  step_roofline  t_roof = useful FLOPs / sustained tensor peak + algorithmic
+               bytes of the memory-bound kernels / measured copy bandwidth,
+               and t_roof / measured step time (frac; frac_graph for the
+               graph replay).
   graph        the same step captured once in a CUDA graph and replayed.
   per_model    (default workload only) step ms and useful TFLOP/s with their
                fraction of the measured bf16 peak for each model at each f:
@@ -481,6 +485,18 @@ def run_ours(args, rank, world, device_index):
 
     value = job_tflops(flops_rank, world, ms_max)
     bf16_peak = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    # Step roofline: the GEMM phase at the sustained tensor peak plus the
+    # memory-bound phase at the measured copy bandwidth (the phases are serial
+    # within a group), against the measured step.
+    hbm_bytes = sum(v["algo_bytes"] for v in trace.values() if v["useful_flops"] == 0) / args.steps
+    t_tensor = flops_rank / (bf16_peak * 1e12) * 1e3
+    t_hbm = hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    step_roof = {"t_roof_ms": t_tensor + t_hbm, "tensor_part_ms": t_tensor, "hbm_part_ms": t_hbm,
+                 "useful_tflop": flops_rank / 1e12, "hbm_gb": hbm_bytes / 1e9,
+                 "peak_tflops": bf16_peak, "hbm_gbs": peaks["hbm_gbs"],
+                 "frac": (t_tensor + t_hbm) / ms_max}
+    if graph is not None:
+        step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -495,7 +511,7 @@ def run_ours(args, rank, world, device_index):
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
                    "parallelism": f"{world} independent ranks (no collective on the data path)"},
-        "roofline": roof, "kernels": kernels, "gpu_launches": launches,
+        "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "gpu_launches": launches,
         "gpu_launches_per_step": launches / args.steps, "clocks": clock_info,
     }
     if e2e is not None:
