@@ -288,7 +288,7 @@ cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
   const int detail = trace_detail();
   std::string name = "gemm_tcgen05";
   if (detail >= 1) name = g.mode == kRect ? "gemm:rect" : (g.K == g.M ? "gemm:sym_square" : "gemm:syrk");
-  if (detail >= 2) name += ":" + std::to_string(g.mode == kRect ? g.N : g.M);
+  if (detail >= 2) name += ":" + std::to_string(g.mode == kRect ? std::min(g.M, g.N) : g.M);
   return traced(name, flops, bytes, s, [&] { return launch_gemm(g, st, s); });
 }
 cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
@@ -407,15 +407,25 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     return -1;
   };
   int xcur = 0;  // X[xcur] holds the current Y (wide) or Y^T
-  // D = Y^T Q (L x s): A = Y^T is X[xcur] itself (k > m) or given as its
-  // transpose (wide); B = Q half-stored.
-  auto rect_ytq = [&](int xi) -> GemmDesc {
+  // The product with Q in X's own orientation, written as is (no transposed
+  // store): wide, D = Q Y (s x L) with A = Q half-stored and B = Y^T given as
+  // its transpose, which is X[xi] itself; otherwise D = Y^T Q (L x s) with
+  // A = X[xi] = Y^T and B = Q half-stored.
+  auto rect_q = [&](int xi) -> GemmDesc {
     GemmDesc g{};
-    g.A = p.X[xi]; g.a_bstride = p.x_bs; g.lda = p.mp;
-    g.a_tr = p.wide;
-    g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
-    g.b_half = !dense;
-    g.M = p.L; g.N = p.s; g.K = p.s; g.batch = p.batch;
+    if (p.wide) {
+      g.A = p.S[Q]; g.a_bstride = p.s_bs; g.lda = p.sp;
+      g.a_half = !dense;
+      g.B = p.X[xi]; g.b_bstride = p.x_bs; g.ldb = p.mp;
+      g.b_tr = true;
+      g.M = p.s; g.N = p.L;
+    } else {
+      g.A = p.X[xi]; g.a_bstride = p.x_bs; g.lda = p.mp;
+      g.B = p.S[Q]; g.b_bstride = p.s_bs; g.ldb = p.sp;
+      g.b_half = !dense;
+      g.M = p.L; g.N = p.s;
+    }
+    g.K = p.s; g.batch = p.batch;
     g.mode = kRect; g.alpha = 1.f;
     return g;
   };
@@ -425,14 +435,9 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   const int T = hp.ns_steps, rs = hp.restart_iter;
   for (int t = 1; t <= T; ++t) {
     if (rs > 1 && t == rs) {
-      // Y <- Q Y:  D = Y^T Q (L x s) is the new Y^T; stored in X's
-      // orientation: D^T = the new Y when wide, D itself otherwise.
-      GemmDesc g = rect_ytq(xcur);
-      if (p.wide) {
-        g.outT = p.X[xcur ^ 1]; g.outT_bstride = p.x_bs; g.ld_outT = p.mp;
-      } else {
-        g.out = p.X[xcur ^ 1]; g.out_bstride = p.x_bs; g.ld_out = p.mp;
-      }
+      // Y <- Q Y, in X's orientation.
+      GemmDesc g = rect_q(xcur);
+      g.out = p.X[xcur ^ 1]; g.out_bstride = p.x_bs; g.ld_out = p.mp;
       if ((rc = launch(g)) != DION3_OK) return rc;
       xcur ^= 1;
       if ((rc = launch(sym(nullptr, nullptr, p.S[R], nullptr, 1.f, 0.f, 0.f, xcur))) != DION3_OK) return rc;
@@ -455,13 +460,9 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
       if ((rc = launch(sym(p.S[Z], p.S[tm], p.S[R], nullptr, 1.f, 0.f, 0.f))) != DION3_OK) return rc;
     }
   }
-  // O = Q Y, written as X's k x m orientation.
-  GemmDesc g = rect_ytq(xcur);
-  if (p.wide) {
-    g.outT = out.O; g.outT_bstride = out.o_bs; g.ld_outT = out.ld_o;
-  } else {
-    g.out = out.O; g.out_bstride = out.o_bs; g.ld_out = out.ld_o;
-  }
+  // O = Q Y, written in X's k x m orientation.
+  GemmDesc g = rect_q(xcur);
+  g.out = out.O; g.out_bstride = out.o_bs; g.ld_out = out.ld_o;
   return launch(g);
 }
 

@@ -208,3 +208,25 @@ def test_syrk_diagonal_blocks_whole(cuda_lib, tr):
     got, ref = _np(whole[:, :, :s]), _np(mirrored[:, :, :s])
     assert np.array_equal(got[:, mask], ref[:, mask])
     assert (got[:, ~mask] == 7.0).all()
+
+
+@pytest.mark.parametrize("s,L,batch", [(520, 1000, 2), (1024, 4096, 1), (700, 300, 2)])
+def test_rect_half_a_with_transposed_b(cuda_lib, s, L, batch):
+    """D = Q Y with Q half-stored (A) and B = Y^T passed as its transpose, i.e.
+    Y itself (the product that writes O in Y's orientation): equal to the same
+    product with Q fully stored and Y^T given explicitly."""
+    rng = np.random.default_rng(s + 3 * L)
+    Q = _dev(_sym(rng, batch, s, 1.0 / np.sqrt(s)))
+    Y = _dev(rng.standard_normal((batch, s, L)))
+    Yt = _dev(np.swapaxes(_np(Y[:, :, :L]), 1, 2))
+    ref = _dev(np.zeros((batch, s, L)))
+    d3.gemm_f16(Q[:, :, :s], Yt[:, :, :s], D=ref[:, :, :L])
+    got = _dev(np.zeros((batch, s, L)))
+    d3.gemm_f16(_as_half_stored(Q, s)[:, :, :s], Y[:, :, :L], D=got[:, :, :L],
+                mode=d3.GEMM_RECT | d3.GEMM_A_HALF | d3.GEMM_B_TRANS)
+    torch.cuda.synchronize()
+    g, r = _np(got[:, :, :L]), _np(ref[:, :, :L])
+    assert np.isfinite(g).all()
+    assert np.abs(g - r).max() <= 4e-3 * max(1.0, np.abs(r).max())
+    want = _np(Q[:, :, :s]) @ _np(Y[:, :, :L])
+    assert rel_fro(g, want) < 2e-3
