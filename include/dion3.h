@@ -17,12 +17,17 @@
  *
  * Conventions shared by every entry point:
  *   - Memory: every tensor and the workspace is caller-owned DEVICE memory; the
- *     library never allocates device memory.  Arrays of pointers
- *     (dion3_group.params, ...) are HOST arrays read during the call only.
+ *     library never allocates device memory (its only CUDA objects are a small
+ *     per-device pool of streams and events, made on first use by
+ *     dion3_step / dion3_step_lazy with several groups, and the events of the
+ *     launch trace).  Arrays of pointers (dion3_group.params, ...) are HOST
+ *     arrays read during the call only.
  *   - Layout: matrices are dense row-major with row pitch == cols; each device
  *     pointer must be 16-byte aligned; the workspace 256-byte aligned.
- *   - Ordering: every call only enqueues work on `stream` and returns without
- *     synchronising; results are visible to later work on the same stream.
+ *   - Ordering: every call only enqueues work on `stream` (or on library
+ *     streams forked from it and joined back into it before the call returns)
+ *     and returns without synchronising; results are visible to later work on
+ *     the same stream.
  *     Calls that share one workspace must not overlap on the device.  Since a
  *     call enqueues kernel launches only (no host synchronisation, no
  *     allocation), it can be captured in a CUDA graph and replayed.  The
