@@ -35,8 +35,12 @@ notes of the repository):
   iterations; the pages print none.
 * lr_eff = lr / sqrt(f) (proportionality constant 1: parity unpinned as to the
   constant, since the pages give only the proportionality); no weight decay.
-* NorMuon per-neuron normalisation is mentioned but never defined on the pages;
-  it is NOT part of this oracle.
+* NorMuon per-neuron normalisation is mentioned but never defined on the pages.
+  ``dion3_step`` leaves it out.  ``dion3_step_normuon`` adds it as a reading
+  taken from the NorMuon method itself (PARITY UNPINNED as to the pages: they
+  only say the normalisation is NorMuon's and runs in float32).  The reading's
+  definition is in ``normuon_rows`` / ``normuon_update``; its CPU tests pin the
+  code to that definition (closed forms and invariants), not to the pages.
 * Rounding: M is stored in fp32 (each + and x computed exactly in double, then
   rounded once to fp32 round-to-nearest-even, which equals an fp32 operation);
   the parameter update is computed in double and rounded once to the parameter
@@ -282,3 +286,73 @@ def dion3_step(W: np.ndarray, M: np.ndarray, G: np.ndarray, *, f: float, mu: flo
     W1 = update_rows(W, S, O, lr_eff, param_dtype)
     M2 = decay_rows(M1, S, mu)
     return W1, M2, S, O
+
+
+# ----------------------------------------------------------------------------
+# NorMuon per-neuron normalisation (a reading; parity unpinned as to the pages)
+# ----------------------------------------------------------------------------
+# "Dion3 Cuts Muon Optimizer Time by Up to 6x ...", section "Dion3's fastest
+# path is a combined systems stack": the per-neuron normalisation is inherited
+# from NorMuon; "Dion3: Full-Stack Orthogonal Updates", limitations paragraph:
+# it runs in float32.  Neither page defines it.  The reading, from the NorMuon
+# method: a neuron is a row of W (an output unit); each row i keeps a running
+# second moment v_i of the orthogonalised update's entries, the row is divided
+# by sqrt(v_i) + eps, and the normalised update is rescaled to a fixed RMS.
+# With row selection only the selected rows have an update, so only their v
+# moves (as only their momentum decays), and the RMS is matched over the
+# k x m block that is written.
+
+def normuon_rows(O: np.ndarray, v_sel: np.ndarray, beta2: float, eps: float):
+    """Per-row second moment and normalising factor of the orthogonalised rows.
+
+    O: k x m (one row per selected parameter row), v_sel: the k selected rows'
+    state.  v_i <- beta2 v_i + (1 - beta2) mean_j O_ij^2; d_i = 1 / (sqrt(v_i) +
+    eps).  Returns (d, v_new) in float64 (the stored state is fp32(v_new))."""
+    O = np.asarray(O, dtype=np.float64)
+    ms = np.mean(O * O, axis=1)
+    v_new = float(beta2) * np.asarray(v_sel, dtype=np.float64) + (1.0 - float(beta2)) * ms
+    d = 1.0 / (np.sqrt(v_new) + float(eps))
+    return d, v_new
+
+
+def normuon_update(O: np.ndarray, d: np.ndarray, rms: float) -> np.ndarray:
+    """The normalised update U = g * diag(d) O with g such that ||U||_F =
+    rms * sqrt(k m) (U = 0 when diag(d) O = 0)."""
+    On = np.asarray(O, dtype=np.float64) * np.asarray(d, dtype=np.float64)[:, None]
+    F = float(np.sqrt(np.sum(On * On)))
+    if F == 0.0:
+        return np.zeros_like(On)
+    return (float(rms) * math.sqrt(On.size) / F) * On
+
+
+def dion3_step_normuon(W: np.ndarray, M: np.ndarray, G: np.ndarray, v: np.ndarray, *, f: float,
+                       mu: float, lr: float, beta2: float = 0.95, nm_eps: float = 1e-8,
+                       rms: float = 0.2, eps: float = 1e-7, coeffs=MUON_QUINTIC, steps: int = 5,
+                       param_dtype: str = "bf16", lr_f32: bool = True,
+                       force_selection: np.ndarray | None = None):
+    """``dion3_step`` with the per-neuron normalisation between steps 4 and 5:
+    v[S] <- fp32(beta2 v[S] + (1 - beta2) mean_j O^2), U = normuon_update(O,
+    1 / (sqrt(v[S]) + nm_eps), rms), W[S] <- round_p(W[S] - (lr / sqrt(f)) U).
+    v is the per-row fp32 state (length n); rows outside S keep theirs.
+
+    Returns (W_new, M_new, S, O, v_new fp32)."""
+    n, _ = np.shape(M)
+    M1 = accumulate(M, G)
+    k = num_selected(f, n)
+    if force_selection is None:
+        S = select_rows(row_l1(M1), k)
+    else:
+        S = np.sort(np.asarray(force_selection, dtype=np.int64))
+        assert S.shape == (k,)
+    X = normalize(M1[S], eps)
+    O = newton_schulz(X, coeffs, steps)
+    v_out = np.array(v, dtype=np.float32, copy=True)
+    d, v_new = normuon_rows(O, v_out[S], beta2, nm_eps)
+    v_out[S] = v_new.astype(np.float32)
+    U = normuon_update(O, d, rms)
+    lr_eff = float(lr) / math.sqrt(float(f))
+    if lr_f32:
+        lr_eff = float(np.float32(lr_eff))
+    W1 = update_rows(W, S, U, lr_eff, param_dtype)
+    M2 = decay_rows(M1, S, mu)
+    return W1, M2, S, O, v_out
