@@ -313,12 +313,19 @@ def run_ours(args, rank, world, device_index):
     # Lazy decay (--lazy-decay): per-row pending factors, one [batch, rows]
     # buffer per group, starting at 1.
     scales = [torch.ones((st_["batch"], st_["rows"]), dtype=torch.float32, device=device) for st_ in state]
+    # Per-neuron normalisation (--normuon): per-row second moments, one
+    # [batch, rows] buffer per group, starting at 0.
+    nm = d3.NormuonParams()
+    vstate = [torch.zeros((st_["batch"], st_["rows"]), dtype=torch.float32, device=device) for st_ in state]
 
-    def do_step(grps, scl, sel_out, wsp):
-        if args.lazy_decay:
-            d3.step_lazy(grps, hp, scl, wsp, sel_idx_out=sel_out, stream=stream)
+    def do_step(grps, scl, sel_out, wsp, vst=None, stream_=stream):
+        if args.normuon:
+            d3.step_normuon(grps, hp, nm, vst if vst is not None else vstate, wsp, sel_idx_out=sel_out,
+                            stream=stream_)
+        elif args.lazy_decay:
+            d3.step_lazy(grps, hp, scl, wsp, sel_idx_out=sel_out, stream=stream_)
         else:
-            d3.step(grps, hp, wsp, sel_idx_out=sel_out, stream=stream)
+            d3.step(grps, hp, wsp, sel_idx_out=sel_out, stream=stream_)
 
     def barrier():
         rank_barrier(world)
@@ -358,10 +365,7 @@ def run_ours(args, rank, world, device_index):
         side.wait_stream(stream)
         cg_ = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg_, stream=side):
-            if args.lazy_decay:
-                d3.step_lazy(cgroups, hp, scales, ws, sel_idx_out=sel)   # on the capturing stream
-            else:
-                d3.step(cgroups, hp, ws, sel_idx_out=sel)
+            do_step(cgroups, scales, sel, ws, stream_=None)   # on the capturing stream
         for _ in range(args.warmup):
             cg_.replay()
         barrier()
@@ -421,7 +425,7 @@ def run_ours(args, rank, world, device_index):
                     evs.append(copy_stream.record_event())
             for (gi, lo, hi), ev, sg in zip(pieces, evs, sub_groups):
                 stream.wait_event(ev)
-                do_step([sg], [scales[gi][lo:hi]], [sel[gi][lo:hi]], ws_e2e)
+                do_step([sg], [scales[gi][lo:hi]], [sel[gi][lo:hi]], ws_e2e, [vstate[gi][lo:hi]])
             for x, h in zip(sel, host_sel):
                 h.copy_(x, non_blocking=True)
 
@@ -444,7 +448,8 @@ def run_ours(args, rank, world, device_index):
         del host_g, ws_e2e
 
     per_model = None
-    if args.workload == "7b" and args.f == 0.25 and args.max_batch == 0 and not args.no_per_model:
+    if args.workload == "7b" and args.f == 0.25 and args.max_batch == 0 and not args.no_per_model \
+            and not args.normuon:
         peaks0, _ = load_peaks()
         peak0 = peaks0.get("bf16_tflops_sustained") or peaks0["bf16_tflops"]
         head = {"model": "7B", "f": args.f, "ms_per_step": ms_max,
@@ -507,6 +512,8 @@ def run_ours(args, rank, world, device_index):
                    "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
                    "ns": f"Gram NS T=5 restart@3, {args.ns_dtype} operands, fp32 accumulate",
                    "momentum_decay": "lazy (dion3_step_lazy)" if args.lazy_decay else "eager (dion3_step)",
+                   "normuon": (f"per-neuron normalisation (dion3_step_normuon, NorMuon reading): beta2={nm.beta2}, "
+                               f"eps={nm.eps}, rms={nm.rms}") if args.normuon else None,
                    "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
@@ -709,6 +716,9 @@ def main():
     ap.add_argument("--f", type=float, default=0.25)
     ap.add_argument("--lazy-decay", action="store_true",
                     help="dion3_step_lazy: the selected rows' decay is carried to the next step")
+    ap.add_argument("--normuon", action="store_true",
+                    help="dion3_step_normuon: per-neuron normalisation of the orthogonalised rows "
+                         "(NorMuon reading; the per-model table is skipped)")
     ap.add_argument("--ns-dtype", choices=["f16", "bf16"], default="f16",
                     help="16-bit type of the Gram-NS operands (the pages use fp16)")
     ap.add_argument("--max-batch", type=int, default=0,

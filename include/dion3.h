@@ -366,6 +366,40 @@ dion3_status dion3_step_lazy(const dion3_group* groups, int32_t ngroups,
                              dion3_stream_t stream);
 
 /*
+ * Per-neuron normalisation parameters of dion3_step_normuon.
+ *   beta2  decay of the per-row second moment, 0 <= beta2 < 1 (0.95);
+ *   eps    added to sqrt(v) before dividing, >= 0 (1e-8);
+ *   rms    RMS of the written update block before the learning rate, > 0 (0.2).
+ */
+typedef struct {
+  float beta2;
+  float eps;
+  float rms;
+} dion3_normuon_params;
+
+/*
+ * dion3_step with the per-neuron normalisation that Dion3 inherits from
+ * NorMuon ("Dion3 Cuts Muon Optimizer Time by Up to 6x ...", section "Dion3's
+ * fastest path is a combined systems stack"; in float32 per the limitations
+ * paragraph of "Dion3: Full-Stack Orthogonal Updates").  Neither page defines
+ * it; this entry point implements the NorMuon form as a reading.  Between
+ * (b) and (c), for each matrix with selected rows S and O (k x m):
+ *   v[S_i] <- beta2 v[S_i] + (1 - beta2) mean_j O_ij^2          (fp32)
+ *   d_i = 1 / (sqrt(v[S_i]) + eps),   U = g diag(d) O  with g such that
+ *   ||U||_F = rms sqrt(k m)  (U = 0 when diag(d) O = 0),
+ * and (c) writes W[S] <- W[S] - (lr / sqrt(f)) U.  Rows outside S keep their
+ * v, as they keep their momentum.
+ *   v   host array [ngroups] of device fp32 [batch][rows] state buffers,
+ *       4-byte aligned, zero before the first step; read and written.
+ * Same workspace (dion3_workspace_size), ordering and errors as dion3_step;
+ * the momentum decay is eager.
+ */
+dion3_status dion3_step_normuon(const dion3_group* groups, int32_t ngroups,
+                                const dion3_hparams* hp, const dion3_normuon_params* nm,
+                                float* const* v, void* ws, size_t ws_bytes,
+                                int32_t* const* sel_idx_out, dion3_stream_t stream);
+
+/*
  * Applies pending lazy decays of one shape group: M[b][i] <- fp32(s M[b][i])
  * for every row whose factor s = row_scale[b][i] is not 1, then s <- 1.
  *   momentum   host array [batch] of device fp32 rows x cols matrices.

@@ -40,6 +40,7 @@ EXPORTED = (
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
     "dion3_trace_collect", "dion3_select_rows_noalloc", "dion3_ns_useful_flops",
     "dion3_ns_workspace_size", "dion3_ns_batched", "dion3_step_lazy", "dion3_flush_row_scale",
+    "dion3_step_normuon",
 )
 
 
@@ -64,6 +65,10 @@ class _Group(ctypes.Structure):
                 ("params", ctypes.POINTER(ctypes.c_void_p)),
                 ("grads", ctypes.POINTER(ctypes.c_void_p)),
                 ("momentum", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class _NormuonParams(ctypes.Structure):
+    _fields_ = [("beta2", ctypes.c_float), ("eps", ctypes.c_float), ("rms", ctypes.c_float)]
 
 
 class _TraceEntry(ctypes.Structure):
@@ -94,6 +99,9 @@ _SIGS = {
     "dion3_step_lazy": (ctypes.c_int, [ctypes.POINTER(_Group), _i32, ctypes.POINTER(_HParams),
                                        ctypes.POINTER(_vp), _vp, _sz, ctypes.POINTER(_vp), _vp]),
     "dion3_flush_row_scale": (ctypes.c_int, [_i32, _i32, _i32, ctypes.POINTER(_vp), _vp, _vp]),
+    "dion3_step_normuon": (ctypes.c_int, [ctypes.POINTER(_Group), _i32, ctypes.POINTER(_HParams),
+                                          ctypes.POINTER(_NormuonParams), ctypes.POINTER(_vp), _vp, _sz,
+                                          ctypes.POINTER(_vp), _vp]),
     "dion3_gemm_f16": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32,
                                       _vp, _i32, ctypes.c_int64, _vp, _i32, ctypes.c_int64,
                                       _vp, _i32, ctypes.c_int64, _vp, _i32, ctypes.c_int64,
@@ -400,6 +408,35 @@ def step_lazy(groups: Sequence[Group], hp: HParams, row_scale: Sequence, ws,
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     _check(load_library().dion3_step_lazy(cg, len(groups), ctypes.byref(hs), rs, _ptr(ws), nbytes, sel,
                                           _stream(stream)))
+
+
+@dataclass
+class NormuonParams:
+    """Per-neuron normalisation of dion3_step_normuon (NorMuon form, a reading:
+    the pages name it but do not define it)."""
+    beta2: float = 0.95
+    eps: float = 1e-8
+    rms: float = 0.2
+
+    def c_struct(self) -> _NormuonParams:
+        return _NormuonParams(self.beta2, self.eps, self.rms)
+
+
+def step_normuon(groups: Sequence[Group], hp: HParams, nm: NormuonParams, v: Sequence, ws,
+                 sel_idx_out: Optional[Sequence] = None, stream=None, ws_bytes: Optional[int] = None):
+    """dion3_step with the per-neuron normalisation (see dion3_step_normuon):
+    one fp32 [batch, rows] state tensor per group in v, zeros before the first
+    call."""
+    cg = (_Group * len(groups))(*[g.c_struct() for g in groups])
+    hs = hp.c_struct()
+    ns = nm.c_struct()
+    vs = (ctypes.c_void_p * len(groups))(*[_ptr(t) for t in v])
+    sel = None
+    if sel_idx_out is not None:
+        sel = (ctypes.c_void_p * len(groups))(*[_ptr(t) for t in sel_idx_out])
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(load_library().dion3_step_normuon(cg, len(groups), ctypes.byref(hs), ctypes.byref(ns), vs,
+                                             _ptr(ws), nbytes, sel, _stream(stream)))
 
 
 def flush_row_scale(momentum: Sequence, row_scale, stream=None):

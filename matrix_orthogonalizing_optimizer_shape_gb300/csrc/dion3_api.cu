@@ -316,6 +316,15 @@ cudaError_t traced_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const double bytes = static_cast<double>(a.batch) * a.k * a.cols * (2.0 + 2.0 * pb);
   return traced("scatter_update", 0.0, bytes, s, [&] { return launch_scatter(a, vec, s); });
 }
+cudaError_t traced_normuon_rows(const NormRowsArgs& a, bool vec, cudaStream_t s) {
+  // O read once; per row: the index, v read and written, d and rowc written.
+  const double bytes = static_cast<double>(a.batch) * a.k * (2.0 * a.m + 4.0 + 8.0 + 8.0);
+  return traced("normuon_rows", 0.0, bytes, s, [&] { return launch_normuon_rows(a, vec, s); });
+}
+cudaError_t traced_normuon_scale(const NormScaleArgs& a, cudaStream_t s) {
+  const double bytes = static_cast<double>(a.batch) * a.k * 12.0;
+  return traced("normuon_scale", 0.0, bytes, s, [&] { return launch_normuon_scale(a, s); });
+}
 
 // Useful FLOPs of the schedule run_gram_ns() launches (triangle = half).
 double schedule_flops(int k, int m, const dion3_hparams& hp) {
@@ -597,6 +606,8 @@ struct GroupPlan {
   __half* O;
   long long o_bs;
   int ld_o;
+  float* nm_d;     // per-neuron normalisation: row factors [batch][k]
+  float* nm_rowc;  // and the rows' d^2 q [batch][k]
   NsPlan ns;
 };
 
@@ -612,6 +623,8 @@ void plan_group(Carver& c, const dion3_group& g, float f, GroupPlan& gp) {
   gp.ld_o = static_cast<int>(round_up(g.cols, 8));
   gp.o_bs = static_cast<long long>(gp.k) * gp.ld_o;
   gp.O = c.take<__half>(gp.o_bs * g.batch);
+  gp.nm_d = c.take<float>(static_cast<long long>(g.batch) * gp.k);
+  gp.nm_rowc = c.take<float>(static_cast<long long>(g.batch) * gp.k);
   plan_ns(c, gp.k, gp.m, gp.batch, gp.ns);
 }
 
@@ -953,7 +966,8 @@ class GroupStreams {
 // instead of being written back (dion3_step_lazy).
 dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp, void* ws,
                        size_t ws_bytes, int32_t* const* sel_idx_out, float* const* row_scale,
-                       dion3_stream_t stream) {
+                       dion3_stream_t stream, const dion3_normuon_params* nm = nullptr,
+                       float* const* nm_v = nullptr) {
   size_t need = 0;
   dion3_status rc = dion3_workspace_size(groups, ngroups, hp, &need);
   if (rc != DION3_OK) return rc;
@@ -967,6 +981,15 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
     for (int i = 0; i < ngroups; ++i)
       if (row_scale[i] == nullptr || (reinterpret_cast<uintptr_t>(row_scale[i]) & 3u))
         return fail(DION3_ERR_INVALID_ARG, "row_scale[%d] must be a 4-byte aligned device pointer", i);
+  if (nm != nullptr) {
+    if (!(nm->beta2 >= 0.f && nm->beta2 < 1.f) || !(nm->eps >= 0.f) || !(nm->rms > 0.f) ||
+        !std::isfinite(nm->rms) || !std::isfinite(nm->eps))
+      return fail(DION3_ERR_INVALID_ARG, "normuon: need 0 <= beta2 < 1, eps >= 0, finite rms > 0");
+    if (nm_v == nullptr) return fail(DION3_ERR_INVALID_ARG, "normuon: v must not be NULL");
+    for (int i = 0; i < ngroups; ++i)
+      if (nm_v[i] == nullptr || (reinterpret_cast<uintptr_t>(nm_v[i]) & 3u))
+        return fail(DION3_ERR_INVALID_ARG, "v[%d] must be a 4-byte aligned device pointer", i);
+  }
   if ((rc = check_ws(ws, ws_bytes, need)) != DION3_OK) return rc;
   if (inject_launch_fail()) return fail(DION3_ERR_CUDA, "injected launch failure (DION3_INJECT=launch_fail)");
   unsigned* st = device_status_ptr();
@@ -1028,6 +1051,21 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
     }
     NsOut out{gp.O, gp.o_bs, gp.ld_o};
     if ((rc = run_gram_ns(gp.ns, *hp, out, st, s)) != DION3_OK) return rc;
+    if (nm != nullptr) {
+      // Per-neuron normalisation of the k orthogonalised rows (v of the
+      // selected parameter rows, the row factors, scaled to RMS rms).
+      NormRowsArgs na{};
+      na.rows = g.rows; na.k = gp.k; na.m = g.cols; na.batch = g.batch;
+      na.idx = idx; na.O = gp.O; na.o_bstride = gp.o_bs; na.ld_o = gp.ld_o;
+      na.o_bf16 = hp->ns_dtype == DION3_BF16;
+      na.v = nm_v[gi]; na.beta2 = nm->beta2; na.eps = nm->eps;
+      na.d = gp.nm_d; na.rowc = gp.nm_rowc; na.status = st;
+      if ((e = traced_normuon_rows(na, g.cols % 8 == 0 && gp.ld_o % 8 == 0, s)) != cudaSuccess)
+        return cuda_fail(e, "normuon rows launch");
+      NormScaleArgs sc{};
+      sc.k = gp.k; sc.m = g.cols; sc.batch = g.batch; sc.rowc = gp.nm_rowc; sc.d = gp.nm_d; sc.rms = nm->rms;
+      if ((e = traced_normuon_scale(sc, s)) != cudaSuccess) return cuda_fail(e, "normuon scale launch");
+    }
     // (c) scatter update of the selected parameter rows.
     for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
       const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
@@ -1039,6 +1077,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       sa.lr = lr_eff;
       sa.status = st;
       sa.o_bf16 = hp->ns_dtype == DION3_BF16;
+      if (nm != nullptr) sa.row_factor = gp.nm_d + static_cast<size_t>(b0) * gp.k;
       if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
   }
@@ -1059,6 +1098,13 @@ dion3_status dion3_step_lazy(const dion3_group* groups, int32_t ngroups, const d
                              dion3_stream_t stream) {
   if (row_scale == nullptr) return fail(DION3_ERR_INVALID_ARG, "row_scale must not be NULL");
   return step_impl(groups, ngroups, hp, ws, ws_bytes, sel_idx_out, row_scale, stream);
+}
+
+dion3_status dion3_step_normuon(const dion3_group* groups, int32_t ngroups, const dion3_hparams* hp,
+                               const dion3_normuon_params* nm, float* const* v, void* ws, size_t ws_bytes,
+                               int32_t* const* sel_idx_out, dion3_stream_t stream) {
+  if (nm == nullptr) return fail(DION3_ERR_INVALID_ARG, "normuon parameters must not be NULL");
+  return step_impl(groups, ngroups, hp, ws, ws_bytes, sel_idx_out, nullptr, stream, nm, v);
 }
 
 dion3_status dion3_flush_row_scale(int32_t rows, int32_t cols, int32_t batch, float* const* momentum,

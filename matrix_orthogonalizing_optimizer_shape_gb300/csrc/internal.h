@@ -129,8 +129,35 @@ struct ScatterArgs {
   float lr;
   bool o_bf16;                     // O holds bf16 (else fp16)
   unsigned* status;                // device status word (kDevCheck on a bad index)
+  const float* row_factor = nullptr;  // [batch][k]: row i's lr is lr * row_factor[b][i] (null: lr)
 };
 cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s);
+
+// Per-neuron normalisation of the orthogonalised rows (the NorMuon reading):
+// per selected row i of matrix b, with q_i = sum_j O_ij^2,
+//   v[b][S_i] <- beta2 v[b][S_i] + (1 - beta2) q_i / m,
+//   d[b][i] = 1 / (sqrt(v[b][S_i]) + eps),  rowc[b][i] = d^2 q_i.
+struct NormRowsArgs {
+  int rows, k, m, batch;
+  const int32_t* idx;              // [batch][k]
+  const __half* O; long long o_bstride; int ld_o;   // [batch][k][ld_o]
+  bool o_bf16;
+  float* v;                        // [batch][rows] fp32 state
+  float beta2, eps;
+  float* d;                        // [batch][k]
+  float* rowc;                     // [batch][k]
+  unsigned* status;
+};
+cudaError_t launch_normuon_rows(const NormRowsArgs& a, bool vec, cudaStream_t s);
+// Per matrix: F^2 = sum_i rowc[b][i] (fixed order), g = rms sqrt(k m) / F
+// (0 when F = 0), then d[b][i] <- g d[b][i].
+struct NormScaleArgs {
+  int k, m, batch;
+  const float* rowc;
+  float* d;
+  float rms;
+};
+cudaError_t launch_normuon_scale(const NormScaleArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Tensor-core GEMM (gemm_tcgen05.cu): D = A B^T with A [batch][M][K] and

@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(256) sumsq_f16_kernel(const __half* X, long lo
 // ---------------------------------------------------------------------------
 // a7: W[S_i] <- round_p(W[S_i] - lr O[i]).  One warp per selected row.
 // ---------------------------------------------------------------------------
-template <int PD, bool VEC, bool BF16>
+template <int PD, bool VEC, bool BF16, bool NORM = false>
 __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ ScatterArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
   }
   const __half* O = a.O + static_cast<long long>(b) * a.o_bstride + static_cast<size_t>(i) * a.ld_o;
   const int cols = a.cols;
-  const float nlr = -a.lr;
+  const float nlr = NORM ? -(a.lr * a.row_factor[static_cast<size_t>(b) * a.k + i]) : -a.lr;
   if constexpr (PD == kBF16) {
     __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(a.W[b]) + static_cast<size_t>(row) * cols;
     if constexpr (VEC) {
@@ -600,6 +600,85 @@ inline unsigned ceil_div(long long a, long long b) { return static_cast<unsigned
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Per-neuron normalisation (NorMuon reading; "Dion3 Cuts Muon Optimizer Time
+// by Up to 6x ...", section "Dion3's fastest path is a combined systems stack",
+// names it; "Dion3: Full-Stack Orthogonal Updates", limitations paragraph: in
+// float32).  One warp per selected row: the row's sum of squares of O, the
+// running second moment of the row's parameter row, and its factor
+// 1 / (sqrt(v) + eps); then one CTA per matrix sums d^2 q over the rows in a
+// fixed order and scales the factors so that the written block has RMS rms.
+// ---------------------------------------------------------------------------
+template <bool VEC, bool BF16>
+__global__ void __launch_bounds__(256) normuon_rows_kernel(const __grid_constant__ NormRowsArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x % kWarp;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  if (gw >= total) return;
+  const int b = static_cast<int>(gw / a.k);
+  const int i = static_cast<int>(gw % a.k);
+  const int row = a.idx[gw];
+  if (row < 0 || row >= a.rows) {  // never expected: record and skip the access
+    if (lane == 0) atomicOr(a.status, kDevCheck);
+    return;
+  }
+  const __half* O = a.O + static_cast<long long>(b) * a.o_bstride + static_cast<size_t>(i) * a.ld_o;
+  float q = 0.f;
+  if constexpr (VEC) {
+    for (int c = lane * 8; c < a.m; c += kWarp * 8) {
+      const uint4 o = *reinterpret_cast<const uint4*>(O + c);
+      const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = e16x2_to_f32<BF16>(w[j]);
+        q = fmaf(f.x, f.x, q);
+        q = fmaf(f.y, f.y, q);
+      }
+    }
+  } else {
+    for (int c = lane; c < a.m; c += kWarp) {
+      const float f = e16_to_f32<BF16>(__half_as_ushort(O[c]));
+      q = fmaf(f, f, q);
+    }
+  }
+  q = warp_sum(q);
+  if (lane == 0) {
+    float* v = a.v + static_cast<size_t>(b) * a.rows + row;
+    const float vn = __fadd_rn(__fmul_rn(a.beta2, *v), __fmul_rn(1.0f - a.beta2, q / static_cast<float>(a.m)));
+    *v = vn;
+    const float d = 1.0f / (sqrtf(vn) + a.eps);
+    a.d[gw] = d;
+    a.rowc[gw] = d * d * q;
+  }
+}
+
+constexpr int kNormScaleThreads = 256;
+
+__global__ void __launch_bounds__(kNormScaleThreads) normuon_scale_kernel(const __grid_constant__ NormScaleArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float part[kNormScaleThreads / kWarp];
+  __shared__ float g_sh;
+  const int b = blockIdx.x;
+  const float* rc = a.rowc + static_cast<size_t>(b) * a.k;
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < a.k; i += kNormScaleThreads) acc += rc[i];
+  acc = warp_sum(acc);
+  if (threadIdx.x % kWarp == 0) part[threadIdx.x / kWarp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float f2 = 0.f;
+    for (int w = 0; w < kNormScaleThreads / kWarp; ++w) f2 += part[w];
+    g_sh = f2 > 0.f ? a.rms * sqrtf(static_cast<float>(a.k) * static_cast<float>(a.m)) / sqrtf(f2) : 0.f;
+  }
+  __syncthreads();
+  const float g = g_sh;
+  float* d = a.d + static_cast<size_t>(b) * a.k;
+  for (int i = threadIdx.x; i < a.k; i += kNormScaleThreads) d[i] *= g;
+}
+
 cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.rows;
   const bool has_grad = a.G[0] != nullptr;
@@ -659,14 +738,37 @@ cudaError_t launch_sumsq_f16(const __half* X, long long n, int batch, float* par
 cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const long long total = static_cast<long long>(a.batch) * a.k;
   void (*k)(ScatterArgs);
+  const bool norm = a.row_factor != nullptr;
   if (a.param_dtype == kBF16) {
-    if (a.o_bf16) k = vec ? scatter_kernel<kBF16, true, true> : scatter_kernel<kBF16, false, true>;
-    else k = vec ? scatter_kernel<kBF16, true, false> : scatter_kernel<kBF16, false, false>;
+    if (a.o_bf16)
+      k = vec ? (norm ? scatter_kernel<kBF16, true, true, true> : scatter_kernel<kBF16, true, true>)
+              : (norm ? scatter_kernel<kBF16, false, true, true> : scatter_kernel<kBF16, false, true>);
+    else
+      k = vec ? (norm ? scatter_kernel<kBF16, true, false, true> : scatter_kernel<kBF16, true, false>)
+              : (norm ? scatter_kernel<kBF16, false, false, true> : scatter_kernel<kBF16, false, false>);
   } else {
-    if (a.o_bf16) k = vec ? scatter_kernel<kF32, true, true> : scatter_kernel<kF32, false, true>;
-    else k = vec ? scatter_kernel<kF32, true, false> : scatter_kernel<kF32, false, false>;
+    if (a.o_bf16)
+      k = vec ? (norm ? scatter_kernel<kF32, true, true, true> : scatter_kernel<kF32, true, true>)
+              : (norm ? scatter_kernel<kF32, false, true, true> : scatter_kernel<kF32, false, true>);
+    else
+      k = vec ? (norm ? scatter_kernel<kF32, true, false, true> : scatter_kernel<kF32, true, false>)
+              : (norm ? scatter_kernel<kF32, false, false, true> : scatter_kernel<kF32, false, false>);
   }
   return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_normuon_rows(const NormRowsArgs& a, bool vec, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.batch) * a.k;
+  void (*k)(NormRowsArgs);
+  if (a.o_bf16)
+    k = vec ? normuon_rows_kernel<true, true> : normuon_rows_kernel<false, true>;
+  else
+    k = vec ? normuon_rows_kernel<true, false> : normuon_rows_kernel<false, false>;
+  return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_normuon_scale(const NormScaleArgs& a, cudaStream_t s) {
+  return launch_kernel(false, normuon_scale_kernel, dim3(a.batch), dim3(kNormScaleThreads), 0, s, a);
 }
 
 }  // namespace dion3

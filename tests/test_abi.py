@@ -198,3 +198,35 @@ def test_variant_flops_match_oracle(lib, k, m):
     dense = sum(2.0 * s * s * L if op[0] in ("syrk", "rect") else 2.0 * s ** 3 for op in log)
     assert d3.ns_useful_flops(d3.NS_GRAM_DENSE, k, m, hp) == dense
     assert d3.ns_useful_flops(7, k, m, hp) < 0
+
+
+def test_step_normuon_validation(lib):
+    """dion3_step_normuon checks its parameters and state pointers on the host
+    before any launch."""
+    g, keep = _fake_group(64, 48, 2)
+    groups = (d3._Group * 1)(g)
+    need = ctypes.c_size_t(0)
+    hp = _hp(f=0.25)
+    assert lib.dion3_workspace_size(groups, 1, ctypes.byref(hp), ctypes.byref(need)) == d3.OK
+    ws = 0x40000000
+    v_ok = (ctypes.c_void_p * 1)(0x50000000)
+    v_bad = (ctypes.c_void_p * 1)(0x50000002)
+    v_null = (ctypes.c_void_p * 1)(None)
+
+    def call(nm, v):
+        return lib.dion3_step_normuon(groups, 1, ctypes.byref(hp), nm, v, ws, need.value, None, None)
+
+    good = d3._NormuonParams(0.95, 1e-8, 0.2)
+    assert call(None, v_ok) == d3.ERR_INVALID_ARG
+    for bad in ((1.0, 1e-8, 0.2), (-0.1, 1e-8, 0.2), (0.9, -1.0, 0.2), (0.9, 1e-8, 0.0),
+                (0.9, 1e-8, float("inf")), (float("nan"), 1e-8, 0.2)):
+        assert call(ctypes.byref(d3._NormuonParams(*bad)), v_ok) == d3.ERR_INVALID_ARG, bad
+    assert call(ctypes.byref(good), None) == d3.ERR_INVALID_ARG
+    assert call(ctypes.byref(good), v_null) == d3.ERR_INVALID_ARG
+    assert call(ctypes.byref(good), v_bad) == d3.ERR_INVALID_ARG
+    # valid arguments reach the launch stage: the injected failure reports it
+    os.environ["DION3_INJECT"] = "launch_fail"
+    try:
+        assert call(ctypes.byref(good), v_ok) == d3.ERR_CUDA
+    finally:
+        del os.environ["DION3_INJECT"]
