@@ -125,3 +125,49 @@ def test_full_1b_set_fp32_update_matches_oracle_O(cuda_lib):
         O_gpu = (W0[S] - Wg[S]) / lr_eff
         assert rel_fro(O_gpu, O) <= O_REL_FRO, (gi, i, rel_fro(O_gpu, O))
         assert np.array_equal(sets[gi][2][i].cpu().numpy(), M1)
+
+
+def test_full_1b_set_normuon(cuda_lib):
+    """dion3_step_normuon on the full 1B set at f = 1/2 (the NorMuon reading:
+    parity unpinned as to the pages): sampled matrices against the oracle's
+    reading (indices, momentum bit-exact; the selected rows' state v within
+    twice O's tolerance, the others untouched; W within tolerance)."""
+    from oracle import dion3_step_normuon
+    from tests._harness import O_REL_FRO, rel_fro
+    f, lr = 0.5, 0.02
+    nm = d3.NormuonParams()
+    sets = _build("1b", seed=21)
+    samples = {}
+    for gi, (W, G, M) in enumerate(sets):
+        for i in (0, W.shape[0] - 1):
+            samples[(gi, i)] = (W[i].float().cpu().numpy(), G[i].float().cpu().numpy(), M[i].cpu().numpy())
+    hp = d3.HParams(f=f, mu=0.95, lr=lr)
+    cg = [d3.Group(params=list(W.unbind(0)), grads=list(G.unbind(0)), momentum=list(M.unbind(0)))
+          for (W, G, M) in sets]
+    sel = [torch.full((W.shape[0], d3.num_selected(f, W.shape[1])), -1, dtype=torch.int32,
+                      device="cuda") for (W, _, _) in sets]
+    v = [torch.zeros((W.shape[0], W.shape[1]), dtype=torch.float32, device="cuda") for (W, _, _) in sets]
+    ws = d3.alloc_workspace(d3.workspace_size(cg, hp))
+    d3.step_normuon(cg, hp, nm, v, ws, sel_idx_out=sel)
+    d3.device_status()
+    f32 = float(np.float32(f))
+    for (gi, i), (W0, G0, M0) in samples.items():
+        W, G, M = sets[gi]
+        idx = sel[gi][i].cpu().numpy()
+        k = idx.shape[0]
+        l1 = row_l1(accumulate(M0, G0))
+        force = None
+        if boundary_gap(l1, k) < SEL_GAP:
+            assert valid_topk(l1, idx, k)
+            force = idx
+        v0 = np.zeros(W.shape[1], np.float32)
+        W1, M1, S, _, v1 = dion3_step_normuon(W0, M0, G0, v0, f=f32, mu=0.95, lr=lr, beta2=nm.beta2,
+                                              nm_eps=nm.eps, rms=nm.rms, param_dtype="bf16",
+                                              force_selection=force)
+        assert np.array_equal(idx, S), (gi, i)
+        assert np.array_equal(M[i].cpu().numpy(), M1), (gi, i)
+        vg = v[gi][i].cpu().numpy()
+        rest = np.setdiff1d(np.arange(vg.size), S)
+        assert not vg[rest].any()
+        assert rel_fro(vg[S], v1[S]) < 2 * O_REL_FRO, (gi, i)
+        assert_close_wm(W[i].float().cpu().numpy(), W1, f"1b normuon group {gi} matrix {i}")
