@@ -25,9 +25,15 @@ Printed (rank 0, one JSON line):
                and t_roof / measured step time (frac; frac_graph for the
                graph replay).
   graph        the same step captured once in a CUDA graph and replayed.
+  paths        the two parts of the step against their own rooflines: the
+               Gram-NS path (all GEMM launches) in useful TFLOP/s as a fraction
+               of the measured sustained and burst bf16 peaks, and the
+               select/update path (the memory-bound kernels) in GB/s as a
+               fraction of the measured HBM copy bandwidth.
   per_model    (default workload only) step ms and useful TFLOP/s with their
                fraction of the measured bf16 peak for each model at each f:
-               7B at f = 1/4 (the headline) and 1/8, 1B at f = 1, 1/2, 1/4.
+               7B at f = 1/4 (the headline) and 1/8, 1B at f = 1, 1/2, 1/4,
+               each with its `paths` fractions (3 extra traced steps).
 
 --impl reference times the CPU oracle (the only reference this method has:
 there is no reference implementation to install) on the same workload and
@@ -273,9 +279,56 @@ def time_steps(state, hp, d3, device, stream, world, steps, warmup, lazy):
     return max_over_ranks(ms, world, device)
 
 
+def path_fractions(trace, steps, peaks):
+    """The two parts of the step measured against their own roofline, from a
+    launch trace of `steps` steps: the Gram-NS path (every tcgen05 GEMM launch,
+    timed per Newton-Schulz chain) in useful TFLOP/s against the measured
+    sustained and burst bf16 peaks, and the select/update path (the memory-bound
+    kernels) in algorithmic GB/s against the measured HBM copy bandwidth."""
+    gemm = [v for v in trace.values() if v["useful_flops"] > 0]
+    mem = [v for v in trace.values() if v["useful_flops"] == 0]
+    g_ms = sum(v["total_ms"] for v in gemm)
+    g_fl = sum(v["useful_flops"] for v in gemm)
+    m_ms = sum(v["total_ms"] for v in mem)
+    m_b = sum(v["algo_bytes"] for v in mem)
+    sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    out = {}
+    if g_ms > 0:
+        tf = g_fl / (g_ms * 1e-3) / 1e12
+        out.update({"gram_ns_ms_per_step": g_ms / steps, "gram_ns_tflops": tf,
+                    "gram_ns_frac_sustained": tf / sus, "gram_ns_frac_burst": tf / peaks["bf16_tflops"]})
+    if m_ms > 0:
+        gbs = m_b / (m_ms * 1e-3) / 1e9
+        out.update({"select_update_ms_per_step": m_ms / steps, "select_update_gbs": gbs,
+                    "select_update_frac_hbm": gbs / peaks["hbm_gbs"]})
+    return out
+
+
+def traced_fractions(state, hp, d3, stream, steps, lazy, peaks):
+    """path_fractions over `steps` extra steps run with the launch trace on (the
+    trace's events cost a little, so the step time itself is taken without it)."""
+    import torch
+    cg = [st_["group"] for st_ in state]
+    ws = d3.alloc_workspace(d3.workspace_size(cg, hp))
+    scales = [torch.ones((st_["batch"], st_["rows"]), dtype=torch.float32, device=ws.device) for st_ in state]
+    d3.trace_enable(True)
+    for _ in range(steps):
+        if lazy:
+            d3.step_lazy(cg, hp, scales, ws, stream=stream)
+        else:
+            d3.step(cg, hp, ws, stream=stream)
+    trace = d3.trace_collect()
+    d3.trace_enable(False)
+    d3.device_status(stream)
+    del ws, scales
+    return path_fractions(trace, steps, peaks)
+
+
 def per_model_table(args, world, device, stream, d3, hp_kwargs, main_state, head_row, peak):
     """ms and useful TFLOP/s of the step for each (model, f) point: the 7B
-    set (already resident) at the other f, then the 1B set, built for it."""
+    set (already resident) at the other f, then the 1B set, built for it; and
+    the Gram-NS and select/update paths of each against their rooflines."""
+    peaks, _ = load_peaks()
     rows = [head_row]
     states = {"7b": main_state}
     for model, f in PER_MODEL_POINTS:
@@ -286,8 +339,10 @@ def per_model_table(args, world, device, stream, d3, hp_kwargs, main_state, head
         flops = useful_flops_total(groups, f, hp_kwargs, d3)
         ms = time_steps(states[model], hp, d3, device, stream, world, args.per_model_steps, 3, args.lazy_decay)
         tflops = job_tflops(flops, world, ms)
-        rows.append({"model": model.upper(), "f": f, "ms_per_step": ms, "useful_tflops": tflops,
-                     "frac_of_fp16_peak": tflops / world / peak})
+        row = {"model": model.upper(), "f": f, "ms_per_step": ms, "useful_tflops": tflops,
+               "frac_of_fp16_peak": tflops / world / peak}
+        row.update(traced_fractions(states[model], hp, d3, stream, 3, args.lazy_decay, peaks))
+        rows.append(row)
     return rows
 
 
@@ -443,7 +498,9 @@ def run_ours(args, rank, world, device_index):
         e2e = {"value": job_tflops(flops_rank, world, ems), "unit": "TFLOP/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "method": f"pinned host gradients copied on a side stream in sub-batches of <= {chunk} "
-                         "matrices, each sub-batch stepped as soon as it lands; selected rows read back",
+                         "matrices, each sub-batch stepped as soon as it lands; the selected row indices "
+                         "read back to pinned host memory; W and M (the optimizer state) stay resident in "
+                         "HBM, as in training",
                "h2d_gbs": h2d / (ems * 1e-3) / 1e9}
         del host_g, ws_e2e
 
@@ -455,6 +512,7 @@ def run_ours(args, rank, world, device_index):
         head = {"model": "7B", "f": args.f, "ms_per_step": ms_max,
                 "useful_tflops": job_tflops(flops_rank, world, ms_max),
                 "frac_of_fp16_peak": job_tflops(flops_rank, world, ms_max) / world / peak0}
+        head.update(path_fractions(trace, args.steps, peaks0))
         per_model = per_model_table(args, world, device, stream, d3, hp_kwargs, state, head, peak0)
 
     if rank != 0:
@@ -473,6 +531,10 @@ def run_ours(args, rank, world, device_index):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "peak_kind": f"hbm copy ({peak_src})"}
     roof["frac"] = achieved / peak
+    if roof["bound"] == "tensor":
+        # the same rate against the burst figure (a kernel timed on its own)
+        roof["peak_burst"] = peaks["bf16_tflops"]
+        roof["frac_burst"] = achieved / peaks["bf16_tflops"]
     roof["kernel"] = dom_name
     roof["launches_per_step"] = dom["launches"] / args.steps
     tr = traffic_record(dom_name)
@@ -502,6 +564,7 @@ def run_ours(args, rank, world, device_index):
                  "frac": (t_tensor + t_hbm) / ms_max}
     if graph is not None:
         step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
+    paths = path_fractions(trace, args.steps, peaks)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -518,7 +581,8 @@ def run_ours(args, rank, world, device_index):
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
                    "parallelism": f"{world} independent ranks (no collective on the data path)"},
-        "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "gpu_launches": launches,
+        "roofline": roof, "step_roofline": step_roof, "paths": paths, "kernels": kernels,
+        "gpu_launches": launches,
         "gpu_launches_per_step": launches / args.steps, "clocks": clock_info,
     }
     if e2e is not None:

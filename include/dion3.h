@@ -43,6 +43,12 @@
  *     second); a wait that runs out records DION3_ERR_TIMEOUT in a device
  *     status word that dion3_device_status() reads.
  *   - Exceptions never cross this boundary.
+ *   - Per-device state: the library looks up, once per device, the device
+ *     addresses of its own static device variables (the status word, the
+ *     scratch of dion3_select_rows_noalloc) and keeps them, with its stream
+ *     pool, for the life of the process.  After cudaDeviceReset on a device
+ *     those addresses are stale, so a process must not call the library on
+ *     that device again.
  */
 #ifndef DION3_H_
 #define DION3_H_
@@ -304,7 +310,9 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
  * must not exceed 1048576; larger requests return DION3_ERR_INVALID_ARG and
  * enqueue nothing.  No cudaMalloc, cudaFree or other allocating call is made.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture begins.
+ * device current and keeps it; make that first call before any stream capture
+ * begins, and do not call this entry point on a device after cudaDeviceReset
+ * (the kept address would be stale).
  * Every call on a device shares the array and leaves its contents behind
  * (nothing in it needs to start at zero); calls whose work overlaps on the GPU
  * race on it, so order them on one stream.
@@ -368,7 +376,8 @@ dion3_status dion3_step_lazy(const dion3_group* groups, int32_t ngroups,
 /*
  * Per-neuron normalisation parameters of dion3_step_normuon.
  *   beta2  decay of the per-row second moment, 0 <= beta2 < 1 (0.95);
- *   eps    added to sqrt(v) before dividing, >= 0 (1e-8);
+ *   eps    added to sqrt(v) before dividing, > 0 (1e-8; 0 is refused, since a
+ *          selected row whose orthogonalised values are all zero has v = 0);
  *   rms    RMS of the written update block before the learning rate, > 0 (0.2).
  */
 typedef struct {
@@ -408,6 +417,19 @@ dion3_status dion3_step_normuon(const dion3_group* groups, int32_t ngroups,
 dion3_status dion3_flush_row_scale(int32_t rows, int32_t cols, int32_t batch,
                                    float* const* momentum, float* row_scale,
                                    dion3_stream_t stream);
+
+/*
+ * The bounded device-side wait of the tensor-core kernels, run on its own (a
+ * diagnostic of the timeout path; the paper has no counterpart).  One thread
+ * initialises an mbarrier in shared memory and waits for its first phase with
+ * the wait the GEMM uses, giving up after limit_ns nanoseconds of the GPU's
+ * global timer.  With arrive != 0 the thread arrives on the barrier first and
+ * the wait succeeds at once.  With arrive == 0 nothing completes the phase:
+ * the wait runs out, records DION3_ERR_TIMEOUT in the device status word (see
+ * dion3_device_status) and the kernel returns.  No copy or MMA is in flight.
+ *   limit_ns  1000 <= limit_ns <= 1e9, else DION3_ERR_INVALID_ARG.
+ */
+dion3_status dion3_wait_probe(int32_t arrive, int64_t limit_ns, dion3_stream_t stream);
 
 /*
  * Synchronises `stream`, reads and clears the device status word written by

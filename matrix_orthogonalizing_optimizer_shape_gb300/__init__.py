@@ -16,7 +16,6 @@ Typical use::
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from dataclasses import dataclass, field
 from typing import Optional, Sequence
@@ -40,7 +39,7 @@ EXPORTED = (
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
     "dion3_trace_collect", "dion3_select_rows_noalloc", "dion3_ns_useful_flops",
     "dion3_ns_workspace_size", "dion3_ns_batched", "dion3_step_lazy", "dion3_flush_row_scale",
-    "dion3_step_normuon",
+    "dion3_step_normuon", "dion3_wait_probe",
 )
 
 
@@ -116,6 +115,7 @@ _SIGS = {
     "dion3_select_rows_noalloc": (ctypes.c_int, [_i32, _i32, _i32, ctypes.POINTER(_vp),
                                                  ctypes.POINTER(_vp), _i32, _i32, _vp, _vp, _vp]),
     "dion3_trace_collect": (ctypes.c_int, [ctypes.POINTER(_TraceEntry), _i32, ctypes.POINTER(_i32)]),
+    "dion3_wait_probe": (ctypes.c_int, [_i32, ctypes.c_int64, _vp]),
 }
 
 _LIB = None
@@ -447,11 +447,13 @@ def flush_row_scale(momentum: Sequence, row_scale, stream=None):
     _check(load_library().dion3_flush_row_scale(rows, cols, n, M, _ptr(row_scale), _stream(stream)))
 
 
+def wait_probe(arrive: bool, limit_ns: int, stream=None):
+    """Run the library's bounded device-side wait on its own (dion3_wait_probe):
+    with ``arrive`` False the wait runs out after ``limit_ns`` and the next
+    :func:`device_status` raises the timeout."""
+    _check(load_library().dion3_wait_probe(1 if arrive else 0, int(limit_ns), _stream(stream)))
+
+
 def device_status(stream=None):
     """Synchronise and raise if a bounded device-side wait ran out."""
     _check(load_library().dion3_device_status(_stream(stream)))
-
-
-def lr_effective(lr: float, f: float) -> float:
-    """The applied learning rate lr / sqrt(f) (as the host passes it)."""
-    return lr / math.sqrt(f)

@@ -982,9 +982,11 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       if (row_scale[i] == nullptr || (reinterpret_cast<uintptr_t>(row_scale[i]) & 3u))
         return fail(DION3_ERR_INVALID_ARG, "row_scale[%d] must be a 4-byte aligned device pointer", i);
   if (nm != nullptr) {
-    if (!(nm->beta2 >= 0.f && nm->beta2 < 1.f) || !(nm->eps >= 0.f) || !(nm->rms > 0.f) ||
+    // eps > 0 keeps d = 1 / (sqrt(v) + eps) finite for a selected row whose
+    // orthogonalised values are all zero (v = 0 there).
+    if (!(nm->beta2 >= 0.f && nm->beta2 < 1.f) || !(nm->eps > 0.f) || !(nm->rms > 0.f) ||
         !std::isfinite(nm->rms) || !std::isfinite(nm->eps))
-      return fail(DION3_ERR_INVALID_ARG, "normuon: need 0 <= beta2 < 1, eps >= 0, finite rms > 0");
+      return fail(DION3_ERR_INVALID_ARG, "normuon: need 0 <= beta2 < 1, finite eps > 0, finite rms > 0");
     if (nm_v == nullptr) return fail(DION3_ERR_INVALID_ARG, "normuon: v must not be NULL");
     for (int i = 0; i < ngroups; ++i)
       if (nm_v[i] == nullptr || (reinterpret_cast<uintptr_t>(nm_v[i]) & 3u))
@@ -1211,6 +1213,17 @@ dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32
   *count = static_cast<int32_t>(agg.size());
   for (int i = 0; i < static_cast<int>(agg.size()) && i < capacity; ++i) out[i] = agg[i];
   trace_clear_locked();
+  return ok();
+}
+
+dion3_status dion3_wait_probe(int32_t arrive, int64_t limit_ns, dion3_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000LL)
+    return fail(DION3_ERR_INVALID_ARG, "limit_ns must lie in [1e3, 1e9]");
+  unsigned* st = device_status_ptr();
+  if (st == nullptr) return fail(DION3_ERR_CUDA, "cannot resolve the device status word");
+  const cudaError_t e = launch_wait_probe(arrive != 0, static_cast<unsigned long long>(limit_ns), st,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
   return ok();
 }
 

@@ -137,6 +137,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -149,12 +153,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Bounded wait for the phase of `bar` with the given parity.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+// Bounded wait for the phase of `bar` with the given parity: gives up after
+// `limit_ns` of %globaltimer, recording kDevTimeout in the status word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(status, kDevTimeout);
       return false;
     }
@@ -828,6 +834,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// The bounded wait on its own: one thread initialises an mbarrier (count 1),
+// optionally arrives on it, and waits for its first phase with the GEMM's
+// bounded wait and the given limit.  Without the arrival nothing completes the
+// phase, so the wait runs out, records kDevTimeout and the kernel returns.  No
+// copy or MMA is ever in flight here.
+__global__ void __launch_bounds__(32, 1) wait_probe_kernel(unsigned long long limit_ns, int arrive,
+                                                           unsigned* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  if (arrive) mbar_arrive_local(b);
+  mbar_wait(b, 0u, status, limit_ns);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -918,6 +940,10 @@ int max_active_clusters(int dev) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_probe(bool arrive, unsigned long long limit_ns, unsigned* status, cudaStream_t s) {
+  return launch_kernel(false, wait_probe_kernel, dim3(1), dim3(32), 0, s, limit_ns, arrive ? 1 : 0, status);
+}
 
 bool gemm_check(const GemmDesc& g, const char** why) {
   auto fail = [&](const char* m) {

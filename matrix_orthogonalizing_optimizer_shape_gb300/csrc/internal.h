@@ -199,6 +199,11 @@ struct GemmDesc {
 bool gemm_check(const GemmDesc& g, const char** why);
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s);
 
+// One thread waits on an mbarrier with the GEMM's bounded wait and the given
+// limit; without `arrive` nothing completes the barrier and the wait runs out
+// (kDevTimeout in *status).  A diagnostic of the timeout path.
+cudaError_t launch_wait_probe(bool arrive, unsigned long long limit_ns, unsigned* status, cudaStream_t s);
+
 // Status word address on the current device (set up by the API unit).
 unsigned* device_status_ptr();
 

@@ -18,7 +18,10 @@
 //
 // Set-up: the first call on each device, with that device current, asks the
 // CUDA runtime for the array's device address (cudaGetSymbolAddress) and keeps
-// it; make that first call before any stream capture begins.  No call
+// it; make that first call before any stream capture begins.  The kept
+// address belongs to the module loaded in the device's context: after a
+// cudaDeviceReset it is stale, so this entry point must not be called on that
+// device again in the same process.  No call
 // allocates: there is no cudaMalloc, cudaFree or allocating library routine on
 // this path.
 //

@@ -218,7 +218,8 @@ def test_step_normuon_validation(lib):
 
     good = d3._NormuonParams(0.95, 1e-8, 0.2)
     assert call(None, v_ok) == d3.ERR_INVALID_ARG
-    for bad in ((1.0, 1e-8, 0.2), (-0.1, 1e-8, 0.2), (0.9, -1.0, 0.2), (0.9, 1e-8, 0.0),
+    # eps = 0 is refused: a selected row whose O is zero would get d = 1 / 0.
+    for bad in ((1.0, 1e-8, 0.2), (-0.1, 1e-8, 0.2), (0.9, -1.0, 0.2), (0.9, 0.0, 0.2), (0.9, 1e-8, 0.0),
                 (0.9, 1e-8, float("inf")), (float("nan"), 1e-8, 0.2)):
         assert call(ctypes.byref(d3._NormuonParams(*bad)), v_ok) == d3.ERR_INVALID_ARG, bad
     assert call(ctypes.byref(good), None) == d3.ERR_INVALID_ARG
@@ -230,3 +231,9 @@ def test_step_normuon_validation(lib):
         assert call(ctypes.byref(good), v_ok) == d3.ERR_CUDA
     finally:
         del os.environ["DION3_INJECT"]
+
+
+def test_wait_probe_validation(lib):
+    """dion3_wait_probe refuses a limit outside [1 us, 1 s] before any launch."""
+    for bad in (0, 999, 10**9 + 1, -5):
+        assert lib.dion3_wait_probe(0, bad, None) == d3.ERR_INVALID_ARG, bad

@@ -117,3 +117,12 @@ def test_gram_ns_bf16_matches_oracle(cuda_lib, k, m):
     for b in range(2):
         want = newton_schulz(normalize(Xv[b], hp.eps), MUON_QUINTIC, 5)
         assert rel_fro(Og[b], want) <= tol, (k, m, b, rel_fro(Og[b], want))
+
+
+def test_gram_ns_s4096_single(cuda_lib):
+    """A Gram side of 4096 (the s = 4096, aspect 1 point of the Gram-NS sweep):
+    one 4096 x 4096 fp16 Gaussian matrix against the float64 oracle."""
+    X = _inputs(1, 4096, 4096, seed=4096)
+    O = _run(X, d3.HParams())
+    want = newton_schulz(normalize(X[0], 1e-7), MUON_QUINTIC, 5)
+    assert rel_fro(O[0], want) <= O_REL_FRO

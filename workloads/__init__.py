@@ -129,6 +129,26 @@ def device_gaussian_(t, sigma: float, seed: int):
     return t
 
 
+def device_gapped_before_(M, G, seed: int):
+    """Fill the device tensor ``M`` (fp32, n x m) with a previous momentum such
+    that the momentum after the next accumulation, M + G, has Gaussian rows whose
+    l1 norms follow ``ladder(n, seed)`` times m sqrt(2/pi): the gapped-ladder
+    structure (row-norm gaps far above fp32 rounding) on the values that are
+    selected from.  The target rows are drawn and rescaled on the device in
+    double and ``G`` is taken off them, so the fp32 sum the step forms lies
+    within a unit in the last place of the target.  For the model-shaped sets,
+    which are too large to build on the host."""
+    import torch
+    n, m = M.shape
+    g = torch.Generator(device=M.device)
+    g.manual_seed(int(seed))
+    target = torch.randn((n, m), generator=g, device=M.device, dtype=torch.float64)
+    l1_target = torch.from_numpy(ladder(n, seed) * m * math.sqrt(2.0 / math.pi)).to(M.device)
+    target.mul_((l1_target / target.abs().sum(dim=1))[:, None])
+    M.copy_(target.sub_(G.to(torch.float64)))
+    return M
+
+
 SWEEP_S = (1024, 2048, 4096, 8192, 16384)
 SWEEP_ASPECT = (1, 2, 4, 8)
 SWEEP_BATCH = (1, 4, 16, 64)
