@@ -74,49 +74,62 @@ def test_gram_ns_output_singular_values_band(cuda_lib):
     assert sv.min() > 0.6 and sv.max() < 1.25
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
-@pytest.mark.parametrize("k,m", [(200, 520), (520, 200), (256, 256)])
-def test_ns_variants_match_oracle(cuda_lib, variant, k, m):
-    # Gram NS (symmetric / dense) and standard NS (symmetric / dense) on the
-    # same kernels all compute the oracle's standard quintic NS.
-    X = _inputs(2, k, m, seed=variant * 100 + k)
-    hp = d3.HParams()
-    Xd = torch.from_numpy(X).to("cuda").half().contiguous()
+def _variant_err(variant, k, m, ns_dtype, seed):
+    """Largest relative Frobenius error of a Newton-Schulz variant over a batch
+    of two Gaussian k x m matrices (rounded to the 16-bit type), against the
+    oracle's float64 standard quintic NS of the same values."""
+    tdt = torch.bfloat16 if ns_dtype == d3.BF16 else torch.float16
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((2, k, m)).astype(np.float32)
+    hp = d3.HParams(ns_dtype=ns_dtype)
+    Xd = torch.from_numpy(X).to("cuda").to(tdt).contiguous()
     O = torch.full_like(Xd, float("nan"))
     ws = d3.alloc_workspace(d3.ns_workspace_size(variant, k, m, 2, hp))
     d3.ns_batched(variant, Xd, O, hp, ws)
     d3.device_status()
-    O = O.float().cpu().numpy()
-    # The product path (variant 0) is held to the step's tolerance.  The other
-    # variants are timing references: the dense ones do not mirror products, so
-    # the fp16 asymmetry of Z Q and R Z feeds into later products, and standard
-    # NS rounds the rectangular iterate five times; they are held to 5e-2.
-    tol = O_REL_FRO if variant == 0 else 5e-2
-    for b in range(2):
-        want = newton_schulz(normalize(X[b], hp.eps), MUON_QUINTIC, 5)
-        assert rel_fro(O[b], want) <= tol, (variant, k, m, b)
-
-
-@pytest.mark.parametrize("k,m", [(64, 256), (256, 64), (200, 520), (1024, 4096), (128, 128)])
-def test_gram_ns_bf16_matches_oracle(cuda_lib, k, m):
-    # bf16 operands (ns_dtype = BF16): the unit roundoff is 8x that of fp16
-    # (2^-8 vs 2^-11), and the error grows accordingly (about 1e-2 here against
-    # about 1e-3 for fp16).  Rectangular shapes stay within the step's 3e-2;
-    # square ones (the least well-conditioned) are held to 8 x 3e-2.
-    rng = np.random.default_rng(k * 3 + m)
-    X = rng.standard_normal((2, k, m)).astype(np.float32)
-    hp = d3.HParams(ns_dtype=d3.BF16)
-    Xd = torch.from_numpy(X).to("cuda").to(torch.bfloat16).contiguous()
-    O = torch.full_like(Xd, float("nan"))
-    ws = d3.alloc_workspace(d3.gram_ns_workspace_size(k, m, 2, hp))
-    d3.gram_ns_batched(Xd, O, hp, ws)
-    d3.device_status()
     Xv = Xd.float().cpu().numpy().astype(np.float64)
     Og = O.float().cpu().numpy()
-    tol = O_REL_FRO if k != m else 8 * O_REL_FRO
-    for b in range(2):
-        want = newton_schulz(normalize(Xv[b], hp.eps), MUON_QUINTIC, 5)
-        assert rel_fro(Og[b], want) <= tol, (k, m, b, rel_fro(Og[b], want))
+    assert np.isfinite(Og).all()
+    return max(rel_fro(Og[b], newton_schulz(normalize(Xv[b], hp.eps), MUON_QUINTIC, 5)) for b in range(2))
+
+
+# Variants and shapes held to the north star's 3e-2: Gram NS (symmetric
+# products) in fp16 everywhere; standard NS (symmetric or dense products) in
+# fp16 and bf16 everywhere; dense Gram NS in fp16 and symmetric Gram NS in bf16
+# on rectangular shapes.
+_MEETS = ([(d3.F16, v, k, m) for v in (0, 2, 3) for (k, m) in ((200, 520), (520, 200), (256, 256), (128, 128))]
+          + [(d3.BF16, v, k, m) for v in (2, 3) for (k, m) in ((200, 520), (520, 200), (256, 256), (128, 128))]
+          + [(d3.F16, 1, k, m) for (k, m) in ((200, 520), (520, 200), (512, 2048))]
+          + [(d3.BF16, 0, k, m) for (k, m) in ((64, 256), (256, 64), (200, 520), (1024, 4096))])
+
+
+@pytest.mark.parametrize("ns_dtype,variant,k,m", _MEETS)
+def test_ns_variants_within_north_star_tolerance(cuda_lib, ns_dtype, variant, k, m):
+    err = _variant_err(variant, k, m, ns_dtype, seed=k * 3 + m + variant)
+    assert err <= O_REL_FRO, (ns_dtype, variant, k, m, err)
+
+
+# Variants that do NOT meet the north star's 3e-2 on square shapes (the
+# smallest singular values of a square Gaussian matrix are tiny, and a Gram
+# matrix kept in 16 bits loses sigma^2 below the format's precision):
+#   * dense Gram NS (every tile, products of two different matrices not
+#     mirrored, so their 16-bit asymmetry feeds into later products): fp16
+#     2.9e-2 (128 x 128) and 3.4e-2 (256 x 256) measured; bf16 0.06-0.26;
+#   * symmetric Gram NS in bf16 (8 significant bits against fp16's 11): 5.8e-2
+#     (128 x 128), 5.4e-2 (256 x 256), 3.3e-2 (1024 x 1024) measured.
+# These are comparison paths (the Dion3 step runs symmetric Gram NS in fp16, as
+# the pages do).  The test holds them to the measured error with a 1.5x margin
+# so that a regression still shows; it does not claim the north-star bound.
+_DECLARED = [(d3.F16, 1, 128, 128, 2.9e-2), (d3.F16, 1, 256, 256, 3.4e-2),
+             (d3.BF16, 1, 200, 520, 8.7e-2), (d3.BF16, 1, 256, 256, 2.6e-1),
+             (d3.BF16, 0, 128, 128, 5.8e-2), (d3.BF16, 0, 256, 256, 5.4e-2),
+             (d3.BF16, 0, 1024, 1024, 3.3e-2)]
+
+
+@pytest.mark.parametrize("ns_dtype,variant,k,m,measured", _DECLARED)
+def test_ns_variants_outside_north_star_tolerance_as_declared(cuda_lib, ns_dtype, variant, k, m, measured):
+    err = _variant_err(variant, k, m, ns_dtype, seed=k * 3 + m + variant)
+    assert err <= 1.5 * measured, (ns_dtype, variant, k, m, err)
 
 
 def test_gram_ns_s4096_single(cuda_lib):
