@@ -92,11 +92,9 @@ def test_concurrent_groups_match_in_order(cuda_lib):
 
 def test_trace_counts_launches_and_work(cuda_lib):
     """The launch trace over one step: each Newton-Schulz run's 18 GEMMs
-    (T = 5, restart before iteration 3) go out as one chained launch (18
-    launches with DION3_CHAIN=0), with the useful FLOPs 6 s^2 L + 14 s^3 per
-    matrix; every memory-bound kernel launches once per group."""
-    import os
-    chained = os.environ.get("DION3_CHAIN", "1") != "0"
+    (T = 5, restart before iteration 3) are timed as one chain but counted as
+    18 launches, with the useful FLOPs 6 s^2 L + 14 s^3 per matrix; every
+    memory-bound kernel launches once per group."""
     f = 0.25
     hp = d3.HParams(f=f, mu=0.95, lr=0.02)
     groups, _, _, sels = _build(f, seed=31)
@@ -110,7 +108,7 @@ def test_trace_counts_launches_and_work(cuda_lib):
         d3.trace_enable(False)
     d3.device_status()
     gemm = trace["gemm_tcgen05"]
-    assert gemm["launches"] == (1 if chained else 18) * len(SHAPES)
+    assert gemm["launches"] == 18 * len(SHAPES)
     want = 0.0
     for n, m, batch, _ in SHAPES:
         k = d3.num_selected(f, n)
