@@ -955,7 +955,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kp.done != nullptr) {
         unsigned* const cur_done = kp.done + static_cast<size_t>(bidx) * kp.nprod + ur.p;
         const bool defer = ur.next_first > u + nclusters;
-        __syncwarp();  // every lane's (fenced) element-wise stores precede lane 0's count
         if (lane == 0) {
           // Exactly kChunks groups per tile (empty ones where a chunk wrote
           // nothing), so "all but the four most recent" is the previous tile.
