@@ -906,9 +906,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
         if (!tma_ok) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
-          // In a chain these plain stores are counted with the tile (lane 0's
-          // release after the warp barrier below): fence them at GPU scope.
-          if (kp.done != nullptr) __threadfence();
           continue;
         }
         const uint32_t buf = my_staging;
@@ -1294,7 +1291,10 @@ cudaError_t launch_gemm_chain(const GemmDesc* gs, int n, unsigned* done, unsigne
   for (int i = 0; i < n; ++i) {
     if (gs[i].batch != batch || gs[i].elem != gs[0].elem) return cudaErrorInvalidValue;
     if ((e = build_prod(gs[i], mt, dt, kp.prod[i])) != cudaSuccess) return e;
+    // Chains use bulk stores only: a completed bulk group is what the
+    // completion counts wait for.
     const ProdDesc& d = kp.prod[i];
+    if ((d.out != nullptr && d.mOut < 0) || (d.outT != nullptr && d.mOutT < 0)) return cudaErrorInvalidValue;
     U += d.units;
     umin = std::min(umin, d.units);
   }

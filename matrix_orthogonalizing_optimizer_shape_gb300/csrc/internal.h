@@ -217,7 +217,8 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
 // cooperative launch: product i of a matrix starts once product i - 1 of the
 // same matrix has been written (the Newton-Schulz schedule of a shape group,
 // where each product reads what earlier ones wrote).  `done` is device scratch
-// of batch x n counters, zeroed by the launcher on the stream.
+// of batch x n counters, zeroed by the launcher on the stream.  Every output
+// must admit bulk tensor stores (16-byte aligned, pitches multiples of 8).
 int gemm_chain_max_products();
 cudaError_t launch_gemm_chain(const GemmDesc* gs, int n, unsigned* done, unsigned* dev_status, cudaStream_t s);
 
