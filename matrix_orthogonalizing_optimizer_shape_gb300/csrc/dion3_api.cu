@@ -251,7 +251,6 @@ struct NsPlan {
   __half* X[2];   // ping-pong for the restart (Y <- Q Y reads one, writes the other)
   __half* S[4];   // s x s matrices, half-stored symmetric
   long long x_bs, s_bs;
-  unsigned* done; // completion counters of a chained launch, [batch][max products]
 };
 
 void plan_ns(Carver& c, int k, int m, int batch, NsPlan& p) {
@@ -268,7 +267,6 @@ void plan_ns(Carver& c, int k, int m, int batch, NsPlan& p) {
   p.X[0] = c.take<__half>(p.x_bs * batch);
   p.X[1] = c.take<__half>(p.x_bs * batch);
   for (int i = 0; i < 4; ++i) p.S[i] = c.take<__half>(p.s_bs * batch);
-  p.done = c.take<unsigned>(static_cast<long long>(batch) * gemm_chain_max_products());
 }
 
 // Where the gather kernel writes the normalised rows: X[0], rows only.
@@ -293,72 +291,6 @@ cudaError_t traced_gemm(const GemmDesc& g, unsigned* st, cudaStream_t s) {
   if (detail >= 2) name += ":" + std::to_string(g.mode == kRect ? std::min(g.M, g.N) : g.M);
   return traced(name, flops, bytes, s, [&] { return launch_gemm(g, st, s); });
 }
-cudaError_t traced_chain(const GemmDesc* gs, int n, unsigned* done, unsigned* st, cudaStream_t s) {
-  double flops = 0.0, bytes = 0.0;
-  for (int i = 0; i < n; ++i) {
-    const GemmDesc& g = gs[i];
-    flops += g.mode == kSymLower ? static_cast<double>(g.M) * g.M * g.K * g.batch : 2.0 * g.M * g.N * g.K * g.batch;
-    bytes += 2.0 * g.batch * (static_cast<double>(g.M) * g.K + static_cast<double>(g.N) * g.K);
-  }
-  return traced("gemm_tcgen05", flops, bytes, s, [&] { return launch_gemm_chain(gs, n, done, st, s); });
-}
-
-// Whether the GEMMs of a Newton-Schulz run go out as chains (DION3_CHAIN,
-// read once; default on).  Per-launch trace detail times every product on its
-// own, so it uses one launch per product.
-bool chain_enabled() {
-  static const bool on = [] {
-    const char* v = getenv("DION3_CHAIN");
-    return v == nullptr || atoi(v) != 0;
-  }();
-  return on && trace_detail() == 0;
-}
-
-// The GEMMs of one Newton-Schulz run, checked as they are added and launched
-// at the end: as chains of up to gemm_chain_max_products() products, each one
-// cooperative launch in which a product of a matrix waits for the previous
-// product of the same matrix (default), or one launch per product, visiting
-// the batch in alternating order so each launch starts on the matrices the
-// previous one wrote last.
-class GemmRun {
- public:
-  GemmRun(int elem, unsigned* done, unsigned* st, cudaStream_t s) : elem_(elem), done_(done), st_(st), s_(s) {}
-  dion3_status add(const GemmDesc& g0) {
-    GemmDesc g = g0;
-    g.elem = elem_;
-    const char* why = nullptr;
-    if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
-    gs_.push_back(g);
-    return DION3_OK;
-  }
-  dion3_status launch(bool chain) {
-    if (chain) {
-      const int cap = gemm_chain_max_products();
-      for (size_t i = 0; i < gs_.size(); i += cap) {
-        const int n = static_cast<int>(std::min<size_t>(cap, gs_.size() - i));
-        const cudaError_t e = traced_chain(gs_.data() + i, n, done_, st_, s_);
-        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM chain launch");
-      }
-      return DION3_OK;
-    }
-    bool reverse = false;
-    for (GemmDesc& g : gs_) {
-      g.reverse = reverse;
-      reverse = !reverse;
-      const cudaError_t e = traced_gemm(g, st_, s_);
-      if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
-    }
-    return DION3_OK;
-  }
-
- private:
-  int elem_;
-  unsigned* done_;
-  unsigned* st_;
-  cudaStream_t s_;
-  std::vector<GemmDesc> gs_;
-};
-
 cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
   const double gb = a.G[0] == nullptr ? 0.0 : (a.grad_dtype == kBF16 ? 2.0 : 4.0);
   const double wb = a.G[0] == nullptr ? 0.0 : 4.0;
@@ -462,8 +394,18 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
     g.out = D; g.out_bstride = p.s_bs; g.ld_out = p.sp;
     return g;
   };
-  GemmRun run(hp.ns_dtype == DION3_BF16 ? kBF16 : kF16, p.done, st, stream);
-  auto launch = [&](const GemmDesc& g) -> dion3_status { return run.add(g); };
+  bool reverse = false;  // serpentine batch order across the chain
+  auto launch = [&](const GemmDesc& g0) -> dion3_status {
+    GemmDesc g = g0;
+    g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
+    g.reverse = reverse;
+    reverse = !reverse;
+    const char* why = nullptr;
+    if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
+    const cudaError_t e = traced_gemm(g, st, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return DION3_OK;
+  };
   dion3_status rc;
 
   // s x s buffer roles: indices into p.S.
@@ -530,8 +472,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   // O = Q Y, written in X's k x m orientation.
   GemmDesc g = rect_q(xcur);
   g.out = out.O; g.out_bstride = out.o_bs; g.ld_out = out.ld_o;
-  if ((rc = launch(g)) != DION3_OK) return rc;
-  return run.launch(chain_enabled());
+  return launch(g);
 }
 
 // ---------------------------------------------------------------------------
@@ -549,7 +490,6 @@ struct StdPlan {
   __half* Yt[2];
   __half* S[2];
   long long y_bs, yt_bs, s_bs;
-  unsigned* done;
 };
 
 void plan_std(Carver& c, int k, int m, int batch, StdPlan& p) {
@@ -567,7 +507,6 @@ void plan_std(Carver& c, int k, int m, int batch, StdPlan& p) {
   for (int i = 0; i < 2; ++i) p.Y[i] = c.take<__half>(p.y_bs * batch);
   for (int i = 0; i < 2; ++i) p.Yt[i] = c.take<__half>(p.yt_bs * batch);
   for (int i = 0; i < 2; ++i) p.S[i] = c.take<__half>(p.s_bs * batch);
-  p.done = c.take<unsigned>(static_cast<long long>(batch) * gemm_chain_max_products());
 }
 
 void gather_targets_std(const StdPlan& p, GatherArgs& g) {
@@ -583,8 +522,15 @@ void gather_targets_std(const StdPlan& p, GatherArgs& g) {
 dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
                              cudaStream_t stream, bool dense) {
   TraceChain chain("gemm_tcgen05", stream);
-  GemmRun run(hp.ns_dtype == DION3_BF16 ? kBF16 : kF16, p.done, st, stream);
-  auto launch = [&](const GemmDesc& g) -> dion3_status { return run.add(g); };
+  auto launch = [&](const GemmDesc& g0) -> dion3_status {
+    GemmDesc g = g0;
+    g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
+    const char* why = nullptr;
+    if (!gemm_check(g, &why)) return fail(DION3_ERR_INVALID_ARG, "internal GEMM rejected: %s", why);
+    const cudaError_t e = traced_gemm(g, st, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 GEMM launch");
+    return DION3_OK;
+  };
   const int mode_sym = dense ? kRect : kSymLower;
   dion3_status rc;
   for (int t = 0; t < hp.ns_steps; ++t) {
@@ -628,7 +574,7 @@ dion3_status run_standard_ns(const StdPlan& p, const dion3_hparams& hp, const Ns
     }
     if ((rc = launch(g3)) != DION3_OK) return rc;
   }
-  return run.launch(chain_enabled());
+  return DION3_OK;
 }
 
 // Useful FLOPs of each variant (a computed triangle counts half; the dense

@@ -94,50 +94,22 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-// One product of a launch.  A launch runs one product over a batch of
-// matrices, or a chain of products (the Gram Newton-Schulz schedule of one
-// shape group) in which product p of a matrix waits for product p - 1 of the
-// same matrix.
-struct ProdDesc {
-  int mode;                  // kRect / kSymLower
-  int M, N, K;
-  int pairs_r, tiles_c;      // super-tile rows (256) and column tiles (256) of one matrix
-  int units;                 // super-tiles per matrix
-  int mA, mAT, mB, mBT;      // tensor-map indices: K-major (128-row box) and MN-major (64 x 64) tiles
-  int mOut, mOutT;           // store maps (32 x 32 boxes) of out / outT, -1: element-wise stores
-  int a_half, b_half;        // A / B is a half-stored symmetric matrix (M == K / N == K)
-  int a_tr, b_tr;            // A / B is given as its transpose ([K][M] / [K][N]): all tiles MN-major
-  int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
-  int diag_full;             // out_half: diagonal super-tiles written whole, as computed (no mirror)
+struct GemmParams {
+  int M, N, K, mode;
+  int tiles_r, tiles_c;      // row (128) and column (256) tile counts of one matrix
+  int pairs_r;               // super-tile rows (256) of one matrix
+  int units_per_mat, total_units;  // super-tiles per matrix / in the launch
   float alpha, beta, gamma;
   const __half* C; long long c_bs; int ldc;
   __half* out; long long out_bs; int ld_out;
   __half* outT; long long outT_bs; int ld_outT;
-};
-
-constexpr int kMaxProducts = 24;
-constexpr int kMaxMaps = 24;
-
-struct KMaps {
-  CUtensorMap m[kMaxMaps];
-};
-
-// Work of a launch: `batch` matrices x the products' super-tiles, visited in
-// windows of `window` matrices; inside a window product by product, matrix
-// by matrix, super-tile by super-tile.  Unit u belongs to cluster u mod
-// nclusters (every role of both CTAs walks the same sequence).
-struct KParams {
-  int nprod, batch, window;
-  int U;                     // super-tiles per matrix over all products
-  int total_units;
-  int reverse;               // single product: visit the matrices from the last one
-  // Chains: done[b * nprod + p] counts the epilogue warps (8 per CTA, both CTAs
-  // of a pair) that have finished their part of a super-tile of product p of
-  // matrix b; product p of b may start once product p - 1 has reached
-  // 16 x units.  Null for a single product.
-  unsigned* done;
+  int tma_out, tma_outT;     // the output has a TMA store map (16-byte pitch rules hold)
+  int batch, reverse;        // visit matrices from the last one when reverse
+  int a_half, b_half;        // A / B is a half-stored symmetric matrix (M == K / N == K)
+  int a_tr, b_tr;            // A / B is given as its transpose ([K][M] / [K][N]): all tiles MN-major
+  int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
+  int diag_full;             // out_half: diagonal super-tiles written whole, as computed (no mirror)
   unsigned* status;
-  ProdDesc prod[kMaxProducts];
 };
 
 // ---------------------------------------------------------------------------
@@ -236,37 +208,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // None of this thread's bulk groups is still reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Every bulk group of this thread but the four most recent has completed
-// (its writes performed).
-__device__ __forceinline__ void bulk_wait_keep4() { asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); }
-// Orders this thread's global-memory accesses through the generic proxy with
-// those through the async proxy (bulk tensor copies), both ways.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bounded wait (one thread) until *ctr >= target, with acquire semantics at
-// GPU scope; records kDevTimeout and returns false when the limit runs out.
-__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned target, unsigned* status) {
-  if (ld_acquire_gpu(ctr) >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_gpu(ctr) < target) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(status, kDevTimeout);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
-}
 // Generic-proxy shared-memory writes become visible to the async proxy.
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -439,51 +380,20 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // rank r computes row tile 2 P + r.  kSymLower keeps the super-tiles that meet
 // the lower triangle: 256 P + 255 >= 256 bc, i.e. P >= bc, enumerated column by
 // column.
-__device__ __forceinline__ void unit_coords(const ProdDesc& d, int u, int& P, int& bc) {
-  if (d.mode == kSymLower) {
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& P, int& bc) {
+  if (p.mode == kSymLower) {
     bc = 0;
     for (;;) {
-      const int cnt = d.pairs_r - bc;
+      const int cnt = p.pairs_r - bc;
       if (u < cnt) break;
       u -= cnt;
       ++bc;
     }
     P = bc + u;
   } else {
-    P = u / d.tiles_c;
-    bc = u % d.tiles_c;
+    P = u / p.tiles_c;
+    bc = u % p.tiles_c;
   }
-}
-
-// Unit u of the launch -> product, matrix and super-tile, and (for chains)
-// the first unit of the next product of the same matrix: the earliest unit
-// that waits for this one (INT_MAX when no product follows).
-struct UnitRef {
-  int p, bidx, P, bc;
-  int next_first;
-};
-__device__ __forceinline__ UnitRef decode_unit(const KParams& kp, int u) {
-  UnitRef r;
-  const int nwin = (kp.batch + kp.window - 1) / kp.window;
-  int w = u / (kp.window * kp.U);
-  if (w >= nwin) w = nwin - 1;
-  const int m0 = w * kp.window;
-  const int mc = min(kp.window, kp.batch - m0);
-  int o = u - m0 * kp.U;
-  int p = 0;
-  while (p < kp.nprod - 1) {
-    const int blk = mc * kp.prod[p].units;
-    if (o < blk) break;
-    o -= blk;
-    ++p;
-  }
-  const int units = kp.prod[p].units;
-  const int j = o / units;
-  r.p = p;
-  r.bidx = kp.reverse ? kp.batch - 1 - (m0 + j) : m0 + j;
-  r.next_first = p + 1 < kp.nprod ? (u - o) + mc * units + j * kp.prod[p + 1].units : 0x7fffffff;
-  unit_coords(kp.prod[p], o - j * units, r.P, r.bc);
-  return r;
 }
 
 struct Smem {
@@ -549,20 +459,19 @@ __device__ __forceinline__ bool mma_slabs(int kb0, int kb1, uint32_t& kc, uint32
 // all its chunks of a tile before it waits for the accumulator, so the load
 // latency overlaps the MMAs (only when the chunk is full and C's pitch allows
 // vector loads; otherwise chunk_values reads C element-wise).
-__device__ __forceinline__ bool c_vector_ok(const ProdDesc& p, int c0) {
+__device__ __forceinline__ bool c_vector_ok(const GemmParams& p, int c0) {
   return p.C != nullptr && (c0 + 32 <= p.N) && (p.ldc % 8 == 0);
 }
-__device__ __forceinline__ void prefetch_c(const ProdDesc& p, int bidx, int r, int c0, uint4 (&cv)[4]) {
+__device__ __forceinline__ void prefetch_c(const GemmParams& p, int bidx, int r, int c0, uint4 (&cv)[4]) {
   if (c_vector_ok(p, c0) && r < p.M) {
     const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
-    // L2 only: inside a chain another SM wrote C during this launch.
 #pragma unroll
-    for (int q = 0; q < 4; ++q) cv[q] = __ldcg(reinterpret_cast<const uint4*>(crow + 8 * q));
+    for (int q = 0; q < 4; ++q) cv[q] = *reinterpret_cast<const uint4*>(crow + 8 * q);
   }
 }
 
 template <bool BF16>
-__device__ __forceinline__ void chunk_values(const ProdDesc& p, int bidx, int r, int c0, const uint32_t (&v)[32],
+__device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
                                              const uint4 (&cv)[4], uint32_t (&hp)[16]) {
   float f[32];
 #pragma unroll
@@ -583,7 +492,7 @@ __device__ __forceinline__ void chunk_values(const ProdDesc& p, int bidx, int r,
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (c0 + j < p.N) f[j] = fmaf(p.beta, unpack1<BF16>(__half_as_ushort(__ldcg(crow + j))), f[j]);
+        if (c0 + j < p.N) f[j] = fmaf(p.beta, unpack1<BF16>(__half_as_ushort(crow[j])), f[j]);
     }
   }
   if (p.gamma != 0.0f) {
@@ -607,7 +516,7 @@ __device__ __forceinline__ uint16_t half_bits(const uint32_t (&hp)[16], int j) {
 // result (an element is kept when r >= c and mirrored when r > c), or outputs
 // whose pitch a TMA map cannot describe.  row0 is the warp's first row;
 // mirror = false skips the mirror of a symmetric result.
-__device__ __forceinline__ void store_chunk_scalar(const ProdDesc& p, int bidx, int r, int c0, int row0,
+__device__ __forceinline__ void store_chunk_scalar(const GemmParams& p, int bidx, int r, int c0, int row0,
                                                    const uint32_t (&hp)[16], bool mirror) {
   if (r >= p.M) return;
   const bool sym = p.mode == kSymLower && !p.diag_full;
@@ -676,7 +585,10 @@ __device__ __forceinline__ void diag_chunk(uint32_t buf, uint32_t sw, int lane, 
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ KMaps maps, const __grid_constant__ KParams kp) {
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmAT, const __grid_constant__ CUtensorMap tmBT,
+                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutT,
+                        const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -696,11 +608,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // has started (programmatic dependent launch).
   pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nkb = (p.K + BK - 1) / BK;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;  // issues the pair's MMAs
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   constexpr uint16_t kPair = 0x3;
-  unsigned* const status = kp.status;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -731,36 +643,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // elected lane issues the copies ----------------
       uint32_t kc = 0;
       bool ok = true;
-      for (int u = cluster; u < kp.total_units && ok; u += nclusters) {
-        const UnitRef ur = decode_unit(kp, u);
-        const ProdDesc& d = kp.prod[ur.p];
-        const int nkb = (d.K + BK - 1) / BK;
-        // In a chain, product p of a matrix reads what products < p wrote:
-        // wait until product p - 1 of this matrix is complete in both CTAs of
-        // every pair that worked on it.  Lane 0 acquires the count and issues
-        // every copy below, after the proxy fence.
-        if (kp.done != nullptr && ur.p > 0) {
-          bool dep = true;
-          if (lane == 0)
-            dep = wait_counter(kp.done + static_cast<size_t>(ur.bidx) * kp.nprod + ur.p - 1,
-                               16u * static_cast<unsigned>(kp.prod[ur.p - 1].units), status);
-          if (!__shfl_sync(0xffffffffu, dep ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) fence_proxy_async_global();
-        }
-        const int bi = 2 * ur.P + static_cast<int>(rank);
-        const int b_row = ur.bc * BN + static_cast<int>(rank) * (BN / 2);
-        const int a_t0 = first_transposed_slab(d.a_tr, d.a_half, ur.P, nkb);
-        const int b_t0 = first_transposed_slab(d.b_tr, d.b_half, ur.bc, nkb);
-        const CUtensorMap* mA = &maps.m[d.mA];
-        const CUtensorMap* mAT = &maps.m[d.mAT];
-        const CUtensorMap* mB = &maps.m[d.mB];
-        const CUtensorMap* mBT = &maps.m[d.mBT];
+      for (int u = cluster; u < p.total_units && ok; u += nclusters) {
+        const int bidx = p.reverse ? p.batch - 1 - u / p.units_per_mat : u / p.units_per_mat;
+        int P, bc;
+        unit_coords(p, u % p.units_per_mat, P, bc);
+        const int bi = 2 * P + static_cast<int>(rank);
+        const int b_row = bc * BN + static_cast<int>(rank) * (BN / 2);
+        const int a_t0 = first_transposed_slab(p.a_tr, p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_tr, p.b_half, bc, nkb);
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const uint32_t s = kc % kStages, ph = (kc / kStages) & 1u;
-          if (!mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, status)) {
+          if (!mbar_wait_warp(bar_empty + 8 * s, ph ^ 1u, p.status)) {
             ok = false;
             break;
           }
@@ -774,16 +667,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Smem::kStageBytes);
             const uint32_t full_even = map_to_rank(bar_full + 8 * s, 0);
             if (kb >= a_t0) {
-              tma_load_3d_pair(a_dst, mAT, full_even, am, k0, ur.bidx);
-              tma_load_3d_pair(a_dst + Smem::kABytes / 2, mAT, full_even, am + BM / 2, k0, ur.bidx);
+              tma_load_3d_pair(a_dst, &tmAT, full_even, am, k0, bidx);
+              tma_load_3d_pair(a_dst + Smem::kABytes / 2, &tmAT, full_even, am + BM / 2, k0, bidx);
             } else {
-              tma_load_3d_pair(a_dst, mA, full_even, k0, am, ur.bidx);
+              tma_load_3d_pair(a_dst, &tmA, full_even, k0, am, bidx);
             }
             if (kb >= b_t0) {
-              tma_load_3d_pair(b_dst, mBT, full_even, b_row, k0, ur.bidx);
-              tma_load_3d_pair(b_dst + Smem::kBBytes / 2, mBT, full_even, b_row + BN / 4, k0, ur.bidx);
+              tma_load_3d_pair(b_dst, &tmBT, full_even, b_row, k0, bidx);
+              tma_load_3d_pair(b_dst + Smem::kBBytes / 2, &tmBT, full_even, b_row + BN / 4, k0, bidx);
             } else {
-              tma_load_3d_pair(b_dst, mB, full_even, k0, b_row, ur.bidx);
+              tma_load_3d_pair(b_dst, &tmB, full_even, k0, b_row, bidx);
             }
           }
           __syncwarp();
@@ -794,7 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // the bytes of both CTAs).
       for (uint32_t i = 0; leader && i < kStages && i < kc; ++i) {
         const uint32_t last = kc - 1 - i;  // most recent fill of stage last % kStages
-        mbar_wait_warp(bar_full + 8 * (last % kStages), (last / kStages) & 1u, status);
+        mbar_wait_warp(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
       }
     }
   } else if (warp == 1) {
@@ -803,23 +696,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // loop, one elected lane issues ----------------
       uint32_t kc = 0, tc = 0;
       bool ok = true;
-      for (int u = cluster; u < kp.total_units && ok; u += nclusters, ++tc) {
+      for (int u = cluster; u < p.total_units && ok; u += nclusters, ++tc) {
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-        const UnitRef ur = decode_unit(kp, u);
-        const ProdDesc& d = kp.prod[ur.p];
-        const int nkb = (d.K + BK - 1) / BK;
-        const int a_t0 = first_transposed_slab(d.a_tr, d.a_half, ur.P, nkb);
-        const int b_t0 = first_transposed_slab(d.b_tr, d.b_half, ur.bc, nkb);
-        if (!mbar_wait_warp(bar_tempty + 8 * acc, aph ^ 1u, status)) break;
+        int P, bc;
+        unit_coords(p, u % p.units_per_mat, P, bc);
+        const int a_t0 = first_transposed_slab(p.a_tr, p.a_half, P, nkb);
+        const int b_t0 = first_transposed_slab(p.b_tr, p.b_half, bc, nkb);
+        if (!mbar_wait_warp(bar_tempty + 8 * acc, aph ^ 1u, p.status)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + acc * BN;
+        const uint32_t d = tmem + acc * BN;
         // K slabs in up to three ranges of fixed operand orientation.
         const int t1 = a_t0 < b_t0 ? a_t0 : b_t0, t2 = a_t0 < b_t0 ? b_t0 : a_t0;
-        ok = mma_slabs<BF16, false, false>(0, t1, kc, dt, sA, sB, bar_full, bar_empty, status);
+        ok = mma_slabs<BF16, false, false>(0, t1, kc, d, sA, sB, bar_full, bar_empty, p.status);
         if (ok)
-          ok = a_t0 <= b_t0 ? mma_slabs<BF16, true, false>(t1, t2, kc, dt, sA, sB, bar_full, bar_empty, status)
-                            : mma_slabs<BF16, false, true>(t1, t2, kc, dt, sA, sB, bar_full, bar_empty, status);
-        if (ok) ok = mma_slabs<BF16, true, true>(t2, nkb, kc, dt, sA, sB, bar_full, bar_empty, status);
+          ok = a_t0 <= b_t0 ? mma_slabs<BF16, true, false>(t1, t2, kc, d, sA, sB, bar_full, bar_empty, p.status)
+                            : mma_slabs<BF16, false, true>(t1, t2, kc, d, sA, sB, bar_full, bar_empty, p.status);
+        if (ok) ok = mma_slabs<BF16, true, true>(t2, nkb, kc, d, sA, sB, bar_full, bar_empty, p.status);
         if (!ok) break;
         if (elect_one()) mma_commit_pair(bar_tfull + 8 * acc, kPair);
         __syncwarp();
@@ -827,38 +719,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // All MMAs issued by the elected lane complete before TMEM is freed.
       if (elect_one()) mma_commit_pair(bar_drain, 0x1);
       __syncwarp();
-      mbar_wait_warp(bar_drain, 0u, status);
+      mbar_wait_warp(bar_drain, 0u, p.status);
     }
   } else {
     // ---------------- epilogue warps 2 .. 2 + kEpiWarps - 1 ----------------
     const int quad = warp % 4;  // TMEM lanes 32 quad .. 32 quad + 31
     const int col_lo = ((warp - 2) / 4) * (BN * 4 / kEpiWarps);  // this warp's columns of the tile
     constexpr int kChunks = BN * 4 / kEpiWarps / 32;  // 32-column chunks per warp and tile
-    static_assert(kChunks == 4, "the deferred completion count assumes four bulk groups per tile");
     const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * Smem::kWarpStagingBytes;
+    const bool sym = p.mode == kSymLower;
+    // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
+    // of a symmetric result, or outT).
+    const bool want_n = p.out != nullptr;
+    const bool want_t_any = sym || p.outT != nullptr;
+    const bool tma_ok = (!want_n || p.tma_out) && (!want_t_any || (sym ? p.tma_out : p.tma_outT));
+    const CUtensorMap* map_t = sym ? &tmOut : &tmOutT;
     uint32_t staged = 0;  // chunks this warp has staged
     uint32_t tc = 0;
-    // Chains: each super-tile is counted in done[] once its bulk stores have
-    // completed.  Normally the count is deferred to the end of this warp's
-    // next super-tile, so the warp never waits for the stores it has just
-    // issued.  It is sent at once when a super-tile waiting for it comes no
-    // later than the next round of the clusters (first unit of the next product
-    // of the same matrix <= u + nclusters): a deferred count then waits only
-    // for work on units before every unit that waits for it, so the waits
-    // form no cycle.
-    unsigned* prev_done = nullptr;
-    for (int u = cluster; u < kp.total_units; u += nclusters, ++tc) {
-      const UnitRef ur = decode_unit(kp, u);
-      const ProdDesc& p = kp.prod[ur.p];
-      const int bidx = ur.bidx, P = ur.P, bc = ur.bc;
-      const bool sym = p.mode == kSymLower;
-      // Outputs of a staged chunk: the tile itself, and its transpose (the mirror
-      // of a symmetric result, or outT).
-      const bool want_n = p.out != nullptr;
-      const bool want_t_any = sym || p.outT != nullptr;
-      const bool tma_ok = (!want_n || p.mOut >= 0) && (!want_t_any || (sym ? p.mOut >= 0 : p.mOutT >= 0));
-      const CUtensorMap* map_n = p.mOut >= 0 ? &maps.m[p.mOut] : nullptr;
-      const CUtensorMap* map_t = sym ? map_n : (p.mOutT >= 0 ? &maps.m[p.mOutT] : nullptr);
+    for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
+      const int bidx = p.reverse ? p.batch - 1 - u / p.units_per_mat : u / p.units_per_mat;
+      int P, bc;
+      unit_coords(p, u % p.units_per_mat, P, bc);
       const int bi = 2 * P + static_cast<int>(rank);
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
       // The transposed box of this tile: outT, or the mirror of a symmetric
@@ -869,15 +750,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool tri = sym && !p.diag_full;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
-      // In a chain, C was written by an earlier product of this matrix: acquire
-      // the producer's count before reading it.
-      if (p.C != nullptr && kp.done != nullptr && ur.p > 0) {
-        bool dep = true;
-        if (lane == 0)
-          dep = wait_counter(kp.done + static_cast<size_t>(bidx) * kp.nprod + ur.p - 1,
-                             16u * static_cast<unsigned>(kp.prod[ur.p - 1].units), status);
-        if (!__shfl_sync(0xffffffffu, dep ? 1 : 0, 0)) break;
-      }
       // C of every chunk this warp will write (registers; unused entries stay
       // unread, the conditions match the chunk loop below).
       uint4 cvs[kChunks][4];
@@ -886,11 +758,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int c0 = bc * BN + col_lo + 32 * i;
         if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
       }
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, status));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
-      int committed = 0;  // bulk groups committed (by lane 0) for this tile
 #pragma unroll
       for (int i = 0; i < kChunks; ++i) {
         const int cc = col_lo + 32 * i;
@@ -913,10 +784,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (tri && row0 <= c0 + 31) {
           diag_chunk(buf, sw, lane, staged, hp);
           if (lane == 0) {
-            tma_store_3d(map_n, buf, c0, row0, bidx);
+            tma_store_3d(&tmOut, buf, c0, row0, bidx);
             bulk_commit();
           }
-          ++committed;
           ++staged;
           continue;
         }
@@ -940,48 +810,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
-          if (want_n) tma_store_3d(map_n, buf, c0, row0, bidx);
+          if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
           if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
           bulk_commit();
         }
-        ++committed;
         ++staged;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(bar_tempty + 8 * acc, 0));
-      if (kp.done != nullptr) {
-        unsigned* const cur_done = kp.done + static_cast<size_t>(bidx) * kp.nprod + ur.p;
-        const bool defer = ur.next_first > u + nclusters;
-        if (lane == 0) {
-          // Exactly kChunks groups per tile (empty ones where a chunk wrote
-          // nothing), so "all but the four most recent" is the previous tile.
-          for (; committed < kChunks; ++committed) bulk_commit();
-          if (defer) {
-            if (prev_done != nullptr) {
-              bulk_wait_keep4();
-              fence_proxy_async_global();
-              red_release_gpu_add(prev_done, 1u);
-            }
-          } else {
-            bulk_wait_all();
-            fence_proxy_async_global();
-            if (prev_done != nullptr) red_release_gpu_add(prev_done, 1u);
-            red_release_gpu_add(cur_done, 1u);
-          }
-        }
-        __syncwarp();
-        prev_done = defer ? cur_done : nullptr;
-      }
     }
     // Every bulk store has finished before the CTA (and its shared memory)
-    // goes away; in a chain the last tile's completion is counted.
-    if (lane == 0) {
-      bulk_wait_all();
-      if (prev_done != nullptr) {
-        fence_proxy_async_global();
-        red_release_gpu_add(prev_done, 1u);
-      }
-    }
+    // goes away.
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
   tc_fence_before();
@@ -1128,199 +968,95 @@ bool gemm_check(const GemmDesc& g, const char** why) {
   return true;
 }
 
-namespace {
+cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
+  const bool bf16 = g.elem == kBF16;
+  auto kern = bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  static std::once_flag once[64][2];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63][bf16 ? 1 : 0], [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
 
-// The tensor maps of one launch.  Products that read (or write) the same view
-// of the same buffer share an entry, so a whole Newton-Schulz chain fits in
-// the kernel's table.
-class MapTable {
- public:
-  explicit MapTable(KMaps* maps) : maps_(maps) {}
-  // A load map (128-byte swizzle, box 64 columns x box_rows rows); -1 if it
-  // cannot be encoded or the table is full.
-  int load(const __half* ptr, long long bstride, int ld, int rows, int cols, int batch, int box_rows,
-           CUtensorMapDataType dt) {
-    const Key k{ptr, bstride, ld, rows, cols, batch, box_rows};
-    if (const int i = find(k); i >= 0) return i;
-    if (n_ == kMaxMaps || !make_map(&maps_->m[n_], ptr, bstride, ld, rows, cols, batch, box_rows, dt)) return -1;
-    keys_[n_] = k;
-    return n_++;
-  }
-  // A store map (32 x 32 boxes), or -1 where bulk stores cannot be used.
-  int store(const __half* ptr, long long bstride, int ld, int rows, int cols, int batch, CUtensorMapDataType dt) {
-    if (!storable(ptr, ld, bstride, rows, batch)) return -1;
-    const long long bs = bstride > 0 ? bstride : static_cast<long long>(ld) * rows;
-    const Key k{ptr, bs, ld, rows, cols, batch, 0};
-    if (const int i = find(k); i >= 0) return i;
-    if (n_ == kMaxMaps || !make_store_map(&maps_->m[n_], ptr, bs, ld, rows, cols, batch, dt)) return -1;
-    keys_[n_] = k;
-    return n_++;
-  }
- private:
-  struct Key {
-    const void* ptr;
-    long long bstride;
-    int ld, rows, cols, batch, kind;  // kind: box rows of a load map, 0 for a store map
-  };
-  int find(const Key& k) const {
-    for (int i = 0; i < n_; ++i)
-      if (keys_[i].ptr == k.ptr && keys_[i].bstride == k.bstride && keys_[i].ld == k.ld && keys_[i].rows == k.rows &&
-          keys_[i].cols == k.cols && keys_[i].batch == k.batch && keys_[i].kind == k.kind)
-        return i;
-    return -1;
-  }
-  KMaps* maps_;
-  Key keys_[kMaxMaps] = {};
-  int n_ = 0;
-};
-
-// Fills the product descriptor of one GEMM and its tensor maps.  Returns an
-// error if a map cannot be made (or the table is full).
-cudaError_t build_prod(const GemmDesc& g, MapTable& mt, CUtensorMapDataType dt, ProdDesc& d) {
-  d = ProdDesc{};
   // Operand maps: 128-row boxes for K-major tiles, and 64 x 64 boxes of the
-  // same matrices for the MN-major tiles (every map set, so the kernel never
-  // sees an unset one).  An operand given as its transpose is stored [K][M]
-  // (or [K][N]): both of its maps describe that storage (only the 64 x 64 one
-  // is used).
+  // same matrices for the MN-major tiles of half-stored operands (built for
+  // every launch, so the kernel never sees an unset map).
+  // An operand given as its transpose is stored [K][M] (or [K][N]): both of
+  // its maps describe that storage (only the 64 x 64 one is used).
+  CUtensorMap ta, tb, tat, tbt;
   const int a_rows = g.a_tr ? g.K : g.M, a_cols = g.a_tr ? g.M : g.K;
   const int b_rows = g.b_tr ? g.K : g.N, b_cols = g.b_tr ? g.N : g.K;
-  d.mA = mt.load(g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, g.a_tr ? BK : BM, dt);
-  d.mAT = mt.load(g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, BK, dt);
-  d.mB = mt.load(g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, g.b_tr ? BK : BN / 2, dt);
-  d.mBT = mt.load(g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, BK, dt);
-  if (d.mA < 0 || d.mAT < 0 || d.mB < 0 || d.mBT < 0) return cudaErrorInvalidValue;
-  d.mOut = g.out != nullptr ? mt.store(g.out, g.out_bstride, g.ld_out, g.M, g.N, g.batch, dt) : -1;
-  d.mOutT = (g.mode == kRect && g.outT != nullptr)
-                ? mt.store(g.outT, g.outT_bstride, g.ld_outT, g.N, g.M, g.batch, dt)
-                : -1;
-  d.mode = g.mode;
-  d.M = g.M;
-  d.N = g.N;
-  d.K = g.K;
-  const int tiles_r = (g.M + BM - 1) / BM;
-  d.tiles_c = (g.N + BN - 1) / BN;
-  d.pairs_r = (tiles_r + 1) / 2;
-  // BN == 2 BM: super-tile rows and column tiles have the same 256 extent.
-  d.units = g.mode == kSymLower ? d.pairs_r * (d.pairs_r + 1) / 2 : d.pairs_r * d.tiles_c;
-  d.a_half = g.a_half ? 1 : 0;
-  d.b_half = g.b_half ? 1 : 0;
-  d.a_tr = g.a_tr ? 1 : 0;
-  d.b_tr = g.b_tr ? 1 : 0;
-  d.out_half = g.out_half ? 1 : 0;
+  if (!make_map(&ta, g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, g.a_tr ? BK : BM, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, g.b_tr ? BK : BN / 2, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tat, g.A, g.a_bstride, g.lda, a_rows, a_cols, g.batch, BK, dt)) return cudaErrorInvalidValue;
+  if (!make_map(&tbt, g.B, g.b_bstride, g.ldb, b_rows, b_cols, g.batch, BK, dt)) return cudaErrorInvalidValue;
+
+  CUtensorMap to, tt;
+  memset(&to, 0, sizeof to);
+  memset(&tt, 0, sizeof tt);
+  int tma_out = 0, tma_outT = 0;
+  if (storable(g.out, g.ld_out, g.out_bstride, g.M, g.batch) &&
+      make_store_map(&to, g.out, g.out_bstride > 0 ? g.out_bstride : static_cast<long long>(g.ld_out) * g.M,
+                     g.ld_out, g.M, g.N, g.batch, dt))
+    tma_out = 1;
+  if (g.mode == kRect && storable(g.outT, g.ld_outT, g.outT_bstride, g.N, g.batch) &&
+      make_store_map(&tt, g.outT, g.outT_bstride > 0 ? g.outT_bstride : static_cast<long long>(g.ld_outT) * g.N,
+                     g.ld_outT, g.N, g.M, g.batch, dt))
+    tma_outT = 1;
+
+  GemmParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.mode = g.mode;
+  p.tiles_r = (g.M + BM - 1) / BM;
+  p.tiles_c = (g.N + BN - 1) / BN;
+  p.pairs_r = (p.tiles_r + 1) / 2;
+  if (g.mode == kSymLower) {
+    // BN == 2 BM: super-tile rows and column tiles have the same 256 extent.
+    p.units_per_mat = p.pairs_r * (p.pairs_r + 1) / 2;
+  } else {
+    p.units_per_mat = p.pairs_r * p.tiles_c;
+  }
+  const long long total = static_cast<long long>(p.units_per_mat) * g.batch;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.total_units = static_cast<int>(total);
+  p.alpha = g.alpha;
+  p.beta = g.beta;
+  p.gamma = g.gamma;
+  p.C = g.C;
+  p.c_bs = g.c_bstride;
+  p.ldc = g.ldc;
+  p.out = g.out;
+  p.out_bs = g.out_bstride;
+  p.ld_out = g.ld_out;
+  p.outT = g.outT;
+  p.outT_bs = g.outT_bstride;
+  p.ld_outT = g.ld_outT;
+  p.tma_out = tma_out;
+  p.tma_outT = tma_outT;
+  p.batch = g.batch;
+  p.reverse = g.reverse ? 1 : 0;
+  p.a_half = g.a_half ? 1 : 0;
+  p.a_tr = g.a_tr ? 1 : 0;
+  p.b_tr = g.b_tr ? 1 : 0;
+  p.b_half = g.b_half ? 1 : 0;
+  p.out_half = g.out_half ? 1 : 0;
   // A A^T (+ beta C with C = A half-stored, + gamma I): exactly symmetric as
   // computed, so the diagonal super-tiles of a half-stored result need no mirror.
   const bool self = g.A == g.B && g.lda == g.ldb && g.a_bstride == g.b_bstride && g.a_tr == g.b_tr &&
                     g.a_half == g.b_half;
   const bool c_sym = g.C == nullptr || g.beta == 0.0f ||
                      (g.a_half && g.C == g.A && g.ldc == g.lda && g.c_bstride == g.a_bstride);
-  d.diag_full = (g.mode == kSymLower && g.out_half && self && c_sym && diag_full_enabled()) ? 1 : 0;
-  d.alpha = g.alpha;
-  d.beta = g.beta;
-  d.gamma = g.gamma;
-  d.C = g.C;
-  d.c_bs = g.c_bstride;
-  d.ldc = g.ldc;
-  d.out = g.out;
-  d.out_bs = g.out_bstride;
-  d.ld_out = g.ld_out;
-  d.outT = g.outT;
-  d.outT_bs = g.outT_bstride;
-  d.ld_outT = g.ld_outT;
-  return cudaSuccess;
-}
+  p.diag_full = (g.mode == kSymLower && g.out_half && self && c_sym && diag_full_enabled()) ? 1 : 0;
+  p.status = dev_status;
 
-cudaError_t set_smem_attr(bool bf16, int dev) {
-  static std::once_flag once[64][2];
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(once[dev & 63][bf16 ? 1 : 0], [&] {
-    attr_err = cudaFuncSetAttribute(bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
-  });
-  return attr_err;
-}
-
-}  // namespace
-
-cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
-  const bool bf16 = g.elem == kBF16;
-  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  cudaError_t e = set_smem_attr(bf16, dev);
-  if (e != cudaSuccess) return e;
-  KMaps maps;
-  memset(&maps, 0, sizeof maps);
-  MapTable mt(&maps);
-  KParams kp;
-  memset(&kp, 0, sizeof kp);
-  if ((e = build_prod(g, mt, dt, kp.prod[0])) != cudaSuccess) return e;
-  const long long total = static_cast<long long>(kp.prod[0].units) * g.batch;
-  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kp.nprod = 1;
-  kp.batch = g.batch;
-  kp.window = g.batch;
-  kp.U = kp.prod[0].units;
-  kp.total_units = static_cast<int>(total);
-  kp.reverse = g.reverse ? 1 : 0;
-  kp.done = nullptr;
-  kp.status = dev_status;
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
-  return launch_kernel(pdl_enabled(), bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>,
-                       dim3(2 * clusters), dim3(kThreads), Smem::kDyn, s, maps, kp);
-}
-
-int gemm_chain_max_products() { return kMaxProducts; }
-
-cudaError_t launch_gemm_chain(const GemmDesc* gs, int n, unsigned* done, unsigned* dev_status, cudaStream_t s) {
-  if (n < 1 || n > kMaxProducts || done == nullptr) return cudaErrorInvalidValue;
-  const bool bf16 = gs[0].elem == kBF16;
-  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  cudaError_t e = set_smem_attr(bf16, dev);
-  if (e != cudaSuccess) return e;
-  KMaps maps;
-  memset(&maps, 0, sizeof maps);
-  MapTable mt(&maps);
-  KParams kp;
-  memset(&kp, 0, sizeof kp);
-  const int batch = gs[0].batch;
-  long long U = 0;
-  int umin = 0x7fffffff;
-  for (int i = 0; i < n; ++i) {
-    if (gs[i].batch != batch || gs[i].elem != gs[0].elem) return cudaErrorInvalidValue;
-    if ((e = build_prod(gs[i], mt, dt, kp.prod[i])) != cudaSuccess) return e;
-    // Chains use bulk stores only: a completed bulk group is what the
-    // completion counts wait for.
-    const ProdDesc& d = kp.prod[i];
-    if ((d.out != nullptr && d.mOut < 0) || (d.outT != nullptr && d.mOutT < 0)) return cudaErrorInvalidValue;
-    U += d.units;
-    umin = std::min(umin, d.units);
-  }
-  const long long total = U * batch;
-  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int nclusters = max_active_clusters(dev);
-  // Window of matrices: large enough that a product's super-tiles reach the
-  // same matrix's next product about three rounds of the clusters later (so
-  // its producer rarely has to wait), small enough to keep the window's
-  // matrices close in L2.
-  const int window = static_cast<int>(std::min<long long>(batch, std::max(1, (3 * nclusters + umin - 1) / umin)));
-  kp.nprod = n;
-  kp.batch = batch;
-  kp.window = window;
-  kp.U = static_cast<int>(U);
-  kp.total_units = static_cast<int>(total);
-  kp.reverse = 0;
-  kp.done = done;
-  kp.status = dev_status;
-  if ((e = cudaMemsetAsync(done, 0, sizeof(unsigned) * static_cast<size_t>(batch) * n, s)) != cudaSuccess) return e;
-  const int clusters = static_cast<int>(std::min<long long>(total, nclusters));
-  // Cooperative: every CTA of the grid is resident at once, so a super-tile
-  // waiting for another pair's work never holds back a pair that has not
-  // started (the waits form no cycle: each waits only for earlier units).
-  return launch_kernel_ex(false, true, bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>,
-                          dim3(2 * clusters), dim3(kThreads), Smem::kDyn, s, maps, kp);
+  const int grid = 2 * clusters;
+  return launch_kernel(pdl_enabled(), kern, dim3(grid), dim3(kThreads), Smem::kDyn, s, ta, tb, tat, tbt, to, tt, p);
 }
 
 }  // namespace dion3

@@ -26,37 +26,23 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // Whether GEMM launches carry the attribute (DION3_PDL, read once; default on).
 bool pdl_enabled();
 
-// Launch with or without the programmatic-serialization attribute, and
-// optionally as a cooperative launch (every CTA of the grid resident at once).
+// Launch with or without the programmatic-serialization attribute.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_ex(bool pdl, bool coop, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t s, Args&&... args) {
+cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  unsigned n = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   if (pdl) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  if (coop) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
-    ++n;
-  }
-  cfg.attrs = n > 0 ? attr : nullptr;
-  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
-}
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                          Args&&... args) {
-  return launch_kernel_ex(pdl, false, kern, grid, block, smem, s, static_cast<Args&&>(args)...);
 }
 
 // Device status word bits (written by bounded device-side waits and checks).
@@ -212,15 +198,6 @@ struct GemmDesc {
 // tensor maps); returns false with a message if the GEMM cannot be launched.
 bool gemm_check(const GemmDesc& g, const char** why);
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s);
-
-// A chain of n <= gemm_chain_max_products() GEMMs over the same batch, in one
-// cooperative launch: product i of a matrix starts once product i - 1 of the
-// same matrix has been written (the Newton-Schulz schedule of a shape group,
-// where each product reads what earlier ones wrote).  `done` is device scratch
-// of batch x n counters, zeroed by the launcher on the stream.  Every output
-// must admit bulk tensor stores (16-byte aligned, pitches multiples of 8).
-int gemm_chain_max_products();
-cudaError_t launch_gemm_chain(const GemmDesc* gs, int n, unsigned* done, unsigned* dev_status, cudaStream_t s);
 
 // One thread waits on an mbarrier with the GEMM's bounded wait and the given
 // limit; without `arrive` nothing completes the barrier and the wait runs out
