@@ -2,8 +2,8 @@
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel to an object under
 ``_build/`` and linked into ``libdion3.so`` next to this file.  A unit is
-rebuilt only when it, ``csrc/internal.h`` or ``include/dion3.h`` is newer than
-its object.
+rebuilt only when it, a header under ``csrc/`` or ``include/dion3.h`` is newer
+than its object.
 """
 from __future__ import annotations
 
@@ -35,7 +35,8 @@ def _sources():
 
 
 def _headers():
-    return [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "dion3.h")]
+    own = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    return sorted(own) + [os.path.join(ROOT, "include", "dion3.h")]
 
 
 def _stale(obj: str, deps) -> bool:

@@ -297,6 +297,14 @@ cudaError_t traced_accum(const AccumArgs& a, bool vec, cudaStream_t s) {
   const double bytes = static_cast<double>(a.batch) * a.rows * (a.cols * (4.0 + gb + wb) + 8.0);
   return traced("accum_rownorm", 0.0, bytes, s, [&] { return launch_accum_rownorm(a, vec, s); });
 }
+// The rest of a pooled accumulation.  Its trace entry carries the algorithmic
+// bytes of the whole group's accumulation, part of which the streaming warps of
+// the GEMM launches before it have moved.
+cudaError_t traced_accum_pool(const AccumPool& p, cudaStream_t s) {
+  const double gb = p.grad_dtype == kBF16 ? 2.0 : 4.0;
+  const double bytes = static_cast<double>(p.total) * (p.cols * (4.0 + gb + 4.0) + 8.0);
+  return traced("accum_pool", 0.0, bytes, s, [&] { return launch_accum_pool(p, s); });
+}
 cudaError_t traced_topk(const TopkArgs& t, cudaStream_t s) {
   const double bytes = static_cast<double>(t.batch) * (t.rows * 8.0 + t.k * 4.0 + 4.0);
   return traced("topk_select", 0.0, bytes, s, [&] { return launch_topk(t, s); });
@@ -361,7 +369,7 @@ struct NsOut {
 };
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
-                         cudaStream_t stream, bool dense = false) {
+                         cudaStream_t stream, bool dense = false, const AccumPool* pool = nullptr) {
   TraceChain chain("gemm_tcgen05", stream);
   // Symmetric product of two s x s matrices (or, with xi >= 0, the SYRK
   // R = Y Y^T from X[xi]: Y itself when wide, given as its transpose X = Y^T
@@ -398,6 +406,7 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   auto launch = [&](const GemmDesc& g0) -> dion3_status {
     GemmDesc g = g0;
     g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
+    g.pool = pool;  // every launch of the run lends its streaming warps to the pool
     g.reverse = reverse;
     reverse = !reverse;
     const char* why = nullptr;
@@ -608,6 +617,7 @@ struct GroupPlan {
   int ld_o;
   float* nm_d;     // per-neuron normalisation: row factors [batch][k]
   float* nm_rowc;  // and the rows' d^2 q [batch][k]
+  unsigned long long* pool_next;  // row counter when this group's accumulation is pooled
   NsPlan ns;
 };
 
@@ -625,6 +635,7 @@ void plan_group(Carver& c, const dion3_group& g, float f, GroupPlan& gp) {
   gp.O = c.take<__half>(gp.o_bs * g.batch);
   gp.nm_d = c.take<float>(static_cast<long long>(g.batch) * gp.k);
   gp.nm_rowc = c.take<float>(static_cast<long long>(g.batch) * gp.k);
+  gp.pool_next = c.take<unsigned long long>(1);
   plan_ns(c, gp.k, gp.m, gp.batch, gp.ns);
 }
 
@@ -910,6 +921,16 @@ bool group_streams_enabled() {
   return !g_trace_on;
 }
 
+// Whether dion3_step overlaps the accumulation of one shape group with the
+// Newton-Schulz GEMMs of another (DION3_OVERLAP, read once; default on).
+bool overlap_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("DION3_OVERLAP");
+    return v == nullptr || atoi(v) != 0;
+  }();
+  return on;
+}
+
 class GroupStreams {
  public:
   cudaError_t begin(cudaStream_t caller, int ngroups) {
@@ -999,25 +1020,18 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
 
   cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream);
   const float lr_eff = static_cast<float>(static_cast<double>(hp->lr) / std::sqrt(static_cast<double>(hp->f)));
-  // Every group has its own part of the workspace, so the groups are
-  // independent: with more than one, each runs on a stream of its own, forked
-  // from and joined back into the caller's stream (capturable in a graph).
   std::vector<GroupPlan> plans(ngroups);
   {
     Carver c{static_cast<char*>(ws)};
     for (int gi = 0; gi < ngroups; ++gi) plan_group(c, groups[gi], hp->f, plans[gi]);
   }
-  GroupStreams fork;
-  cudaError_t fe = fork.begin(s0, ngroups);
-  if (fe != cudaSuccess) return cuda_fail(fe, "group stream fork");
-  for (int gi = 0; gi < ngroups; ++gi) {
+  auto sel_of = [&](int gi) -> int32_t* {
+    return (sel_idx_out != nullptr && sel_idx_out[gi] != nullptr) ? sel_idx_out[gi] : plans[gi].idx;
+  };
+  // (a) accumulate + norms of group gi, standalone launches.
+  auto accumulate = [&](int gi, cudaStream_t s) -> dion3_status {
     const dion3_group& g = groups[gi];
     const GroupPlan& gp = plans[gi];
-    cudaStream_t s = fork.stream(gi);
-    int32_t* idx = (sel_idx_out != nullptr && sel_idx_out[gi] != nullptr) ? sel_idx_out[gi] : gp.idx;
-    const bool vec = g.cols % 8 == 0;
-    cudaError_t e;
-    // (a) accumulate + norms, then top-k.
     for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
       const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
       AccumArgs a{};
@@ -1029,12 +1043,44 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       a.l1 = gp.l1 + static_cast<size_t>(b0) * g.rows;
       a.sq = gp.sq + static_cast<size_t>(b0) * g.rows;
       if (row_scale != nullptr) a.scale = row_scale[gi] + static_cast<size_t>(b0) * g.rows;
-      if ((e = traced_accum(a, vec, s)) != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
+      const cudaError_t e = traced_accum(a, g.cols % 8 == 0, s);
+      if (e != cudaSuccess) return cuda_fail(e, "accum_rownorm launch");
     }
+    return DION3_OK;
+  };
+  // The same accumulation as a pool of rows (for the streaming warps of the
+  // GEMM launches that run meanwhile): only for groups of <= kPoolMax matrices
+  // whose rows take the vector path.
+  auto poolable = [&](int gi) { return groups[gi].batch <= kPoolMax && groups[gi].cols % 8 == 0; };
+  auto make_pool = [&](int gi, AccumPool& pool) {
+    const dion3_group& g = groups[gi];
+    const GroupPlan& gp = plans[gi];
+    pool.total = static_cast<long long>(g.batch) * g.rows;
+    pool.rows = g.rows;
+    pool.cols = g.cols;
+    pool.grad_dtype = g.grad_dtype == DION3_BF16 ? kBF16 : kF32;
+    pool.next = gp.pool_next;
+    pool.l1 = gp.l1;
+    pool.sq = gp.sq;
+    pool.scale = row_scale != nullptr ? row_scale[gi] : nullptr;
+    for (int b = 0; b < g.batch; ++b) {
+      pool.M[b] = g.momentum[b];
+      pool.G[b] = g.grads[b];
+    }
+  };
+  // Top-k, gather/normalise (+ decay of the selected momentum rows), Gram-NS
+  // (its GEMM launches lending their streaming warps to `pool`), the
+  // per-neuron normalisation if asked, and the scatter update of group gi.
+  auto select_orthogonalise_update = [&](int gi, cudaStream_t s, const AccumPool* pool,
+                                         int pool_gi) -> dion3_status {
+    const dion3_group& g = groups[gi];
+    const GroupPlan& gp = plans[gi];
+    int32_t* idx = sel_of(gi);
+    const bool vec = g.cols % 8 == 0;
+    cudaError_t e;
     TopkArgs t{};
     t.rows = g.rows; t.k = gp.k; t.batch = g.batch; t.l1 = gp.l1; t.sq = gp.sq; t.idx = idx; t.fro2 = gp.fro2;
     if ((e = traced_topk(t, s)) != cudaSuccess) return cuda_fail(e, "topk launch");
-    // (b) gather/normalise (+ decay of the selected momentum rows), Gram-NS.
     for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
       const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
       GatherArgs ga{};
@@ -1051,8 +1097,19 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       if (ga.out_cols != nullptr) ga.out_cols += ga.cols_bstride * b0;
       if ((e = traced_gather(ga, vec, s)) != cudaSuccess) return cuda_fail(e, "gather launch");
     }
+    if (pool != nullptr) {
+      e = cudaMemsetAsync(pool->next, 0, sizeof(unsigned long long), s);
+      if (e != cudaSuccess) return cuda_fail(e, "pool counter reset");
+    }
     NsOut out{gp.O, gp.o_bs, gp.ld_o};
-    if ((rc = run_gram_ns(gp.ns, *hp, out, st, s)) != DION3_OK) return rc;
+    dion3_status rc2 = run_gram_ns(gp.ns, *hp, out, st, s, false, pool);
+    if (rc2 != DION3_OK) return rc2;
+    if (pool != nullptr) {
+      // Rows of the pool the streaming warps did not reach.
+      if ((e = traced_accum_pool(*pool, s)) != cudaSuccess) return cuda_fail(e, "accum_pool launch");
+    } else if (pool_gi >= 0) {
+      if ((rc2 = accumulate(pool_gi, s)) != DION3_OK) return rc2;
+    }
     if (nm != nullptr) {
       // Per-neuron normalisation of the k orthogonalised rows (v of the
       // selected parameter rows, the row factors, scaled to RMS rms).
@@ -1082,6 +1139,45 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       if (nm != nullptr) sa.row_factor = gp.nm_d + static_cast<size_t>(b0) * gp.k;
       if ((e = traced_scatter(sa, vec, s)) != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
+    return DION3_OK;
+  };
+
+  if (ngroups > 1 && overlap_enabled()) {
+    // Accumulation overlapped with Newton-Schulz: the groups run in order on
+    // the caller's stream, the one with the most Newton-Schulz work first.
+    // Only the first group's accumulation stands alone; each later group's is
+    // a pool of rows that the streaming warps of the previous group's GEMM
+    // launches work through while the tensor cores run, and a pool kernel
+    // finishes (its top-k comes after both, in stream order).
+    std::vector<int> order(ngroups);
+    std::vector<double> work(ngroups);
+    for (int gi = 0; gi < ngroups; ++gi) {
+      order[gi] = gi;
+      work[gi] = schedule_flops(plans[gi].k, groups[gi].cols, *hp) * groups[gi].batch;
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work[x] > work[y]; });
+    if ((rc = accumulate(order[0], s0)) != DION3_OK) return rc;
+    for (int i = 0; i < ngroups; ++i) {
+      const int gi = order[i];
+      const int nx = i + 1 < ngroups ? order[i + 1] : -1;
+      AccumPool pool;
+      const bool pooled = nx >= 0 && poolable(nx);
+      if (pooled) make_pool(nx, pool);
+      if ((rc = select_orthogonalise_update(gi, s0, pooled ? &pool : nullptr, nx)) != DION3_OK) return rc;
+    }
+    return ok();
+  }
+
+  // Otherwise every group has its own part of the workspace, so the groups are
+  // independent: with more than one, each runs on a stream of its own, forked
+  // from and joined back into the caller's stream (capturable in a graph).
+  GroupStreams fork;
+  cudaError_t fe = fork.begin(s0, ngroups);
+  if (fe != cudaSuccess) return cuda_fail(fe, "group stream fork");
+  for (int gi = 0; gi < ngroups; ++gi) {
+    cudaStream_t s = fork.stream(gi);
+    if ((rc = accumulate(gi, s)) != DION3_OK) return rc;
+    if ((rc = select_orthogonalise_update(gi, s, nullptr, -1)) != DION3_OK) return rc;
   }
   if ((fe = fork.end()) != cudaSuccess) return cuda_fail(fe, "group stream join");
   return ok();

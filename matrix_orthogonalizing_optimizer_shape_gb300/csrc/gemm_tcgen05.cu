@@ -71,6 +71,7 @@
 // that runs out sets a bit in the device status word and the CTA winds down:
 // the issuing CTA waits (bounded) for its MMAs, both CTAs meet at a cluster
 // barrier before freeing TMEM, and TMEM is freed on every path.
+#include "accum_row.cuh"
 #include "internal.h"
 
 #include <cuda.h>
@@ -90,7 +91,13 @@ constexpr int BK = 64;  // fp16 elements per 128-byte swizzle row
 constexpr int BN = 256;
 constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, each half of the columns
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accumulation
+// Iterations of loads each streaming warp keeps in flight per row (bf16
+// gradients stay packed, so they afford more depth than fp32 ones; deeper
+// ones spill at the kernel's register budget).
+constexpr int kSideUnrollBF16 = 6;
+constexpr int kSideUnrollF32 = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
@@ -110,6 +117,7 @@ struct GemmParams {
   int out_half;              // kSymLower: no mirror outside the diagonal super-tiles
   int diag_full;             // out_half: diagonal super-tiles written whole, as computed (no mirror)
   unsigned* status;
+  AccumPool pool;            // rows for the streaming warps (total 0: none)
 };
 
 // ---------------------------------------------------------------------------
@@ -603,6 +611,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bar_tempty + 2 * 8;
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kStagingBytes + Smem::kBarBytes);
+  // Epilogue warps of this CTA that have finished (the streaming warps stop
+  // taking rows once all have).
+  uint32_t* epi_done = tmem_slot + 1;
 
   // The next kernel on the stream may be scheduled once every CTA of this one
   // has started (programmatic dependent launch).
@@ -625,6 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
+    *epi_done = 0u;
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -720,6 +732,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (elect_one()) mma_commit_pair(bar_drain, 0x1);
       __syncwarp();
       mbar_wait_warp(bar_drain, 0u, p.status);
+    }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ---------------- streaming warps: rows of another shape group's step a0
+    // (M <- M + G and row norms), taken from the pool's counter one at a time
+    // while this CTA's GEMM work lasts; the rest is left for the pool kernel
+    // that follows the GEMM launches ----------------
+    if (p.pool.total > 0) {
+      for (;;) {
+        uint32_t fin = 0;
+        if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(epi_done);
+        if (__shfl_sync(0xffffffffu, fin, 0) >= static_cast<uint32_t>(kEpiWarps)) break;
+        const long long row = accum_pool_next(p.pool);
+        if (row >= p.pool.total) break;
+        if (p.pool.grad_dtype == kBF16)
+          accum_pool_row<kBF16, kSideUnrollBF16>(p.pool, row);
+        else
+          accum_pool_row<kF32, kSideUnrollF32>(p.pool, row);
+      }
     }
   } else {
     // ---------------- epilogue warps 2 .. 2 + kEpiWarps - 1 ----------------
@@ -821,7 +851,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // Every bulk store has finished before the CTA (and its shared memory)
     // goes away.
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) {
+      bulk_wait_all();
+      atomicAdd(epi_done, 1u);
+    }
     __syncwarp();
   }
   tc_fence_before();
@@ -1053,6 +1086,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
                      (g.a_half && g.C == g.A && g.ldc == g.lda && g.c_bstride == g.a_bstride);
   p.diag_full = (g.mode == kSymLower && g.out_half && self && c_sym && diag_full_enabled()) ? 1 : 0;
   p.status = dev_status;
+  if (g.pool != nullptr) p.pool = *g.pool;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;

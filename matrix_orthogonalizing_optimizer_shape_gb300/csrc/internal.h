@@ -71,6 +71,26 @@ struct AccumArgs {
 };
 cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s);
 
+// Step a0 of one shape group as a pool of rows (row id = matrix x rows + row)
+// handed out one at a time by a device counter to whichever warps ask first:
+// the streaming warps of the tensor-core GEMM launches that run meanwhile (see
+// GemmDesc::pool), then launch_accum_pool for whatever is left.  Every row is
+// accumulated exactly once, with the arithmetic of accum_rownorm.
+constexpr int kPoolMax = 128;  // matrices per pool
+struct AccumPool {
+  long long total = 0;                 // batch x rows; 0: no pool
+  int rows = 0, cols = 0;              // cols a multiple of 8 (vector path)
+  int grad_dtype = kBF16;              // kBF16 or kF32
+  unsigned long long* next = nullptr;  // rows handed out so far; zero before the pool's first user
+  float* l1 = nullptr;                 // [batch][rows]
+  float* sq = nullptr;                 // [batch][rows]
+  float* scale = nullptr;              // lazy decay factors [batch][rows], or null
+  float* M[kPoolMax];
+  const void* G[kPoolMax];
+};
+// The rest of a pool: every row the counter has not handed out yet.
+cudaError_t launch_accum_pool(const AccumPool& p, cudaStream_t s);
+
 // a1: top-k rows by l1 (ties to the lower index), indices ascending, and
 // fro2 = sum of sq over the selected rows.
 struct TopkArgs {
@@ -192,6 +212,9 @@ struct GemmDesc {
   // The operand is given as its transpose: A stored [batch][K][M] (lda >= M),
   // B stored [batch][K][N] (ldb >= N); read as MN-major tiles.
   bool a_tr = false, b_tr = false;
+  // Optional: rows of another shape group's step a0 for the launch's
+  // streaming warps to take while the tensor cores work (null: none).
+  const AccumPool* pool = nullptr;
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

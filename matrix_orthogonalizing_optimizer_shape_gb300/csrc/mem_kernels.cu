@@ -6,9 +6,12 @@
 // the paper), third-level paragraph: rows are chosen by l1 norm, k = ceil(f n),
 // only the chosen sub-matrix is orthogonalised and only the matching weight
 // rows are updated; error feedback decays only the chosen momentum rows by mu.
+#include "accum_row.cuh"
 #include "internal.h"
 
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 namespace dion3 {
 namespace {
@@ -47,14 +50,6 @@ __device__ __forceinline__ __half f32_to_e16(float f) {
   else return __float2half_rn(f);
 }
 
-__device__ __forceinline__ float load_grad(const void* g, size_t i, int gd) {
-  if (gd == kBF16) {
-    const uint16_t h = reinterpret_cast<const uint16_t*>(g)[i];
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
-  }
-  return reinterpret_cast<const float*>(g)[i];
-}
-
 // ---------------------------------------------------------------------------
 // a0: M <- M + G and per-row l1 / sum of squares.  One warp per row; the
 // vector path moves 8 elements per lane per iteration (two float4 of M, one
@@ -73,77 +68,31 @@ __global__ void __launch_bounds__(256) accum_rownorm_kernel(const __grid_constan
   const int r = static_cast<int>(gw % a.rows);
   const int cols = a.cols;
   float* __restrict__ Mrow = a.M[b] + static_cast<size_t>(r) * cols;
-  float l1 = 0.f, sq = 0.f;
+  const void* Grow = nullptr;
+  if constexpr (GD == kBF16) Grow = reinterpret_cast<const uint16_t*>(a.G[b]) + static_cast<size_t>(r) * cols;
+  if constexpr (GD == kF32) Grow = reinterpret_cast<const float*>(a.G[b]) + static_cast<size_t>(r) * cols;
   // Pending lazy decay of this row (warp-uniform); only with a gradient.
   const float rs = (GD >= 0 && a.scale != nullptr) ? a.scale[gw] : 1.0f;
-  const bool scaled = rs != 1.0f;
-
-  if constexpr (VEC) {
-    constexpr int U = 2;  // iterations of loads kept in flight (2 measured fastest: more resident warps)
-    const int step = kWarp * 8;
-    for (int c0 = lane * 8; c0 < cols; c0 += step * U) {
-      float m[U][8];
-      float g[U][8];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * step;
-        if (c < cols) {
-          const float4 x0 = *reinterpret_cast<const float4*>(Mrow + c);
-          const float4 x1 = *reinterpret_cast<const float4*>(Mrow + c + 4);
-          m[u][0] = x0.x; m[u][1] = x0.y; m[u][2] = x0.z; m[u][3] = x0.w;
-          m[u][4] = x1.x; m[u][5] = x1.y; m[u][6] = x1.z; m[u][7] = x1.w;
-          if constexpr (GD == kBF16) {
-            const uint16_t* G = reinterpret_cast<const uint16_t*>(a.G[b]) + static_cast<size_t>(r) * cols;
-            bf16x8_to_f32(__ldcs(reinterpret_cast<const uint4*>(G + c)), g[u]);
-          } else if constexpr (GD == kF32) {
-            const float* G = reinterpret_cast<const float*>(a.G[b]) + static_cast<size_t>(r) * cols;
-            const float4 y0 = __ldcs(reinterpret_cast<const float4*>(G + c));
-            const float4 y1 = __ldcs(reinterpret_cast<const float4*>(G + c + 4));
-            g[u][0] = y0.x; g[u][1] = y0.y; g[u][2] = y0.z; g[u][3] = y0.w;
-            g[u][4] = y1.x; g[u][5] = y1.y; g[u][6] = y1.z; g[u][7] = y1.w;
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * step;
-        if (c < cols) {
-          if constexpr (GD >= 0) {
-            if (scaled) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) m[u][j] = __fmul_rn(rs, m[u][j]);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) m[u][j] = __fadd_rn(m[u][j], g[u][j]);
-            *reinterpret_cast<float4*>(Mrow + c) = make_float4(m[u][0], m[u][1], m[u][2], m[u][3]);
-            *reinterpret_cast<float4*>(Mrow + c + 4) = make_float4(m[u][4], m[u][5], m[u][6], m[u][7]);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            l1 += fabsf(m[u][j]);
-            sq = fmaf(m[u][j], m[u][j], sq);
-          }
-        }
-      }
-    }
-  } else {
-    for (int c = lane; c < cols; c += kWarp) {
-      float m = Mrow[c];
-      if constexpr (GD >= 0) {
-        if (scaled) m = __fmul_rn(rs, m);
-        m = __fadd_rn(m, load_grad(a.G[b], static_cast<size_t>(r) * cols + c, GD));
-        Mrow[c] = m;
-      }
-      l1 += fabsf(m);
-      sq = fmaf(m, m, sq);
-    }
-  }
-  l1 = warp_sum(l1);
-  sq = warp_sum(sq);
+  float l1, sq;
+  // 2 iterations of loads in flight measured fastest here (more resident warps).
+  accum_row<VEC, GD, 2>(Mrow, Grow, cols, rs, l1, sq);
   if (lane == 0) {
     a.l1[gw] = l1;
     a.sq[gw] = sq;
-    if (GD >= 0 && a.scale != nullptr && scaled) a.scale[gw] = 1.0f;
+    if (GD >= 0 && a.scale != nullptr && rs != 1.0f) a.scale[gw] = 1.0f;
+  }
+}
+
+// The rows of an accumulation pool that nobody has taken yet: each warp takes
+// rows from the pool's counter until it is exhausted.
+template <int GD>
+__global__ void __launch_bounds__(256) accum_pool_kernel(const __grid_constant__ AccumPool pool) {
+  pdl_trigger();
+  pdl_wait();
+  for (;;) {
+    const long long row = accum_pool_next(pool);
+    if (row >= pool.total) break;
+    accum_pool_row<GD, 2>(pool, row);
   }
 }
 
@@ -690,6 +639,16 @@ cudaError_t launch_accum_rownorm(const AccumArgs& a, bool vec, cudaStream_t s) {
     k = !has_grad ? accum_rownorm_kernel<false, -1>
                   : (a.grad_dtype == kBF16 ? accum_rownorm_kernel<false, kBF16> : accum_rownorm_kernel<false, kF32>);
   return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_accum_pool(const AccumPool& p, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Enough warps to keep HBM busy (8 CTAs of 8 warps per SM), no more than rows.
+  const long long want = std::min<long long>(static_cast<long long>(sms) * 8, ceil_div(p.total, 8));
+  return launch_kernel(false, p.grad_dtype == kBF16 ? accum_pool_kernel<kBF16> : accum_pool_kernel<kF32>,
+                       dim3(static_cast<unsigned>(std::max<long long>(want, 1))), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_flush_scale(const FlushArgs& a, cudaStream_t s) {

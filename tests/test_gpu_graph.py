@@ -62,8 +62,8 @@ def test_graph_replay_matches_eager(cuda_lib, f):
 
 
 def test_concurrent_groups_match_in_order(cuda_lib):
-    """Several groups in one call run on the library's forked streams; with the
-    launch trace enabled they run in order on the caller's stream.  The groups
+    """Several groups in one call, with the launch trace off and on (events
+    between the launches, groups in order on the caller's stream): the groups
     share nothing, so both give bit-identical results."""
     f = 0.25
     hp = d3.HParams(f=f, mu=0.95, lr=0.02)
@@ -117,6 +117,44 @@ def test_trace_counts_launches_and_work(cuda_lib):
         want += d3.useful_flops(k, m, hp) * batch
     assert gemm["useful_flops"] == pytest.approx(want, rel=1e-9)
     assert gemm["total_ms"] > 0
-    for name in ("accum_rownorm", "topk_select", "gather_normalize", "scatter_update"):
+    for name in ("topk_select", "gather_normalize", "scatter_update"):
         assert trace[name]["launches"] == len(SHAPES), name
         assert trace[name]["total_ms"] > 0
+    # Each group's accumulation: standalone, or (overlapped with the previous
+    # group's Newton-Schulz GEMMs) a pool finished by one pool kernel.
+    acc = sum(trace[n]["launches"] for n in ("accum_rownorm", "accum_pool") if n in trace)
+    assert acc == len(SHAPES)
+
+
+@pytest.mark.parametrize("lazy", [False, True])
+def test_overlapped_groups_match_single_group_calls(cuda_lib, lazy):
+    """One call over several groups (each group's accumulation overlapped with
+    the previous group's Newton-Schulz GEMMs: rows taken by the GEMM launches'
+    streaming warps and by the pool kernel) against the same groups stepped one
+    call at a time (standalone accumulation): selections, momenta and
+    parameters bit-identical over three steps."""
+    f = 0.25
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+    multi = _build(f, seed=41)
+    single = _build(f, seed=41)
+    scales = [[torch.ones((b, n), dtype=torch.float32, device="cuda") for (n, m, b, _) in SHAPES]
+              for _ in range(2)]
+    ws_m = d3.alloc_workspace(d3.workspace_size(multi[0], hp))
+    ws_s = [d3.alloc_workspace(d3.workspace_size([g], hp)) for g in single[0]]
+    for _ in range(3):
+        if lazy:
+            d3.step_lazy(multi[0], hp, scales[0], ws_m, sel_idx_out=multi[3])
+        else:
+            d3.step(multi[0], hp, ws_m, sel_idx_out=multi[3])
+        for gi, g in enumerate(single[0]):
+            if lazy:
+                d3.step_lazy([g], hp, [scales[1][gi]], ws_s[gi], sel_idx_out=[single[3][gi]])
+            else:
+                d3.step([g], hp, ws_s[gi], sel_idx_out=[single[3][gi]])
+    torch.cuda.synchronize()
+    d3.device_status()
+    for gi in range(len(SHAPES)):
+        assert np.array_equal(multi[3][gi].cpu().numpy(), single[3][gi].cpu().numpy())
+        for a, b in zip(multi[1][gi] + multi[2][gi], single[1][gi] + single[2][gi]):
+            assert np.array_equal(to_host(a), to_host(b))
+        assert np.array_equal(to_host(scales[0][gi]), to_host(scales[1][gi]))
