@@ -406,7 +406,10 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   auto launch = [&](const GemmDesc& g0) -> dion3_status {
     GemmDesc g = g0;
     g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
-    g.pool = pool;  // every launch of the run lends its streaming warps to the pool
+    // Every launch of the run lends its streaming warps to the pool (limiting
+    // that to the launches with a long K, whose epilogue warps are idle more
+    // of the time, measured no better).
+    g.pool = pool;
     g.reverse = reverse;
     reverse = !reverse;
     const char* why = nullptr;

@@ -702,8 +702,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait_warp(bar_full + 8 * (last % kStages), (last / kStages) & 1u, p.status);
       }
     }
-  } else if (warp == 1) {
-    if (leader) {
+  } else if (warp == 1 && leader) {
+    {
       // ---------------- MMA issuer: the whole warp of the even CTA runs the
       // loop, one elected lane issues ----------------
       uint32_t kc = 0, tc = 0;
@@ -733,11 +733,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       mbar_wait_warp(bar_drain, 0u, p.status);
     }
-  } else if (warp >= 2 + kEpiWarps) {
-    // ---------------- streaming warps: rows of another shape group's step a0
-    // (M <- M + G and row norms), taken from the pool's counter one at a time
-    // while this CTA's GEMM work lasts; the rest is left for the pool kernel
-    // that follows the GEMM launches ----------------
+  } else if (warp >= 2 + kEpiWarps || warp == 1) {
+    // ---------------- streaming warps (and warp 1 of the odd CTA, which
+    // issues no MMAs): rows of another shape group's step a0 (M <- M + G and
+    // row norms), taken from the pool's counter one at a time while this CTA's
+    // GEMM work lasts; the rest is left for the pool kernel that follows the
+    // GEMM launches ----------------
     if (p.pool.total > 0) {
       for (;;) {
         uint32_t fin = 0;
