@@ -304,24 +304,36 @@ def path_fractions(trace, steps, peaks):
     return out
 
 
-def traced_fractions(state, hp, d3, stream, steps, lazy, peaks):
-    """path_fractions over `steps` extra steps run with the launch trace on (the
-    trace's events cost a little, so the step time itself is taken without it)."""
+def traced_alone(state, hp, d3, stream, steps, lazy, overlap_after=True):
+    """A launch trace of `steps` extra steps with the accumulation overlap off,
+    so every kernel does only its own part: the GEMM launches carry no
+    accumulation rows.  The overlap is set back to `overlap_after`."""
     import torch
     cg = [st_["group"] for st_ in state]
     ws = d3.alloc_workspace(d3.workspace_size(cg, hp))
     scales = [torch.ones((st_["batch"], st_["rows"]), dtype=torch.float32, device=ws.device) for st_ in state]
+    d3.set_overlap(False)
     d3.trace_enable(True)
-    for _ in range(steps):
-        if lazy:
-            d3.step_lazy(cg, hp, scales, ws, stream=stream)
-        else:
-            d3.step(cg, hp, ws, stream=stream)
-    trace = d3.trace_collect()
-    d3.trace_enable(False)
+    try:
+        for _ in range(steps):
+            if lazy:
+                d3.step_lazy(cg, hp, scales, ws, stream=stream)
+            else:
+                d3.step(cg, hp, ws, stream=stream)
+        trace = d3.trace_collect()
+    finally:
+        d3.trace_enable(False)
+        d3.set_overlap(overlap_after)
     d3.device_status(stream)
     del ws, scales
-    return path_fractions(trace, steps, peaks)
+    return trace
+
+
+def traced_fractions(state, hp, d3, stream, steps, lazy, peaks, overlap_after=True):
+    """path_fractions over `steps` extra steps, each part on its own (launch
+    trace on, accumulation overlap off; the step time itself is taken without
+    the trace and with the overlap as configured)."""
+    return path_fractions(traced_alone(state, hp, d3, stream, steps, lazy, overlap_after), steps, peaks)
 
 
 def per_model_table(args, world, device, stream, d3, hp_kwargs, main_state, head_row, peak):
@@ -341,7 +353,8 @@ def per_model_table(args, world, device, stream, d3, hp_kwargs, main_state, head
         tflops = job_tflops(flops, world, ms)
         row = {"model": model.upper(), "f": f, "ms_per_step": ms, "useful_tflops": tflops,
                "frac_of_fp16_peak": tflops / world / peak}
-        row.update(traced_fractions(states[model], hp, d3, stream, 3, args.lazy_decay, peaks))
+        row.update(traced_fractions(states[model], hp, d3, stream, 3, args.lazy_decay, peaks,
+                                    overlap_after=not args.no_overlap))
         rows.append(row)
     return rows
 
@@ -353,6 +366,7 @@ def run_ours(args, rank, world, device_index):
     torch.cuda.set_device(device_index)
     device = torch.device("cuda", device_index)
     d3.load_library()
+    d3.set_overlap(not args.no_overlap)
     groups, desc = workload_groups(args.workload, args.max_batch)
     hp_kwargs = dict(mu=0.95, lr=0.02, eps=1e-7, ns_steps=5, restart_iter=3,
                      ns_dtype=d3.BF16 if args.ns_dtype == "bf16" else d3.F16)
@@ -410,6 +424,11 @@ def run_ours(args, rank, world, device_index):
     ms = ev0.elapsed_time(ev1) / args.steps
     ms_max = max_over_ranks(ms, world, device)
     launches = sum(v["launches"] for v in trace.values())
+    # Each part on its own (accumulation overlap off), for the path fractions
+    # and the GEMM's own roofline.
+    alone_steps = 3
+    alone_trace = traced_alone(state, hp, d3, stream, alone_steps, args.lazy_decay,
+                               overlap_after=not args.no_overlap)
 
     # The same step captured once in a CUDA graph and replayed K times: no
     # host launch overhead between the step's kernels (the library enqueues
@@ -512,7 +531,7 @@ def run_ours(args, rank, world, device_index):
         head = {"model": "7B", "f": args.f, "ms_per_step": ms_max,
                 "useful_tflops": job_tflops(flops_rank, world, ms_max),
                 "frac_of_fp16_peak": job_tflops(flops_rank, world, ms_max) / world / peak0}
-        head.update(path_fractions(trace, args.steps, peaks0))
+        head.update(path_fractions(alone_trace, alone_steps, peaks0))
         per_model = per_model_table(args, world, device, stream, d3, hp_kwargs, state, head, peak0)
 
     if rank != 0:
@@ -531,6 +550,9 @@ def run_ours(args, rank, world, device_index):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "peak_kind": f"hbm copy ({peak_src})"}
     roof["frac"] = achieved / peak
+    if "accum_pool" in trace:
+        roof["note"] = ("the GEMM launches also carry the streaming warps that move part of the next "
+                        "shape group's accumulation (see overlap); roofline_alone is the GEMM on its own")
     if roof["bound"] == "tensor":
         # the same rate against the burst figure (a kernel timed on its own)
         roof["peak_burst"] = peaks["bf16_tflops"]
@@ -546,8 +568,10 @@ def run_ours(args, rank, world, device_index):
               "ms_per_step": v["total_ms"] / args.steps, "share": v["total_ms"] / tot_ms}
         if v["useful_flops"] > 0:
             kv["tflops"] = v["useful_flops"] / (v["total_ms"] * 1e-3) / 1e12
-        if v["algo_bytes"] > 0 and v["useful_flops"] == 0:
+        if v["algo_bytes"] > 0 and v["useful_flops"] == 0 and name != "accum_pool":
             kv["gbs"] = v["algo_bytes"] / (v["total_ms"] * 1e-3) / 1e9
+        if name == "accum_pool":
+            kv["note"] = "the rows of the pooled accumulations that the GEMM launches' streaming warps left"
         kernels[name] = kv
 
     value = job_tflops(flops_rank, world, ms_max)
@@ -564,7 +588,29 @@ def run_ours(args, rank, world, device_index):
                  "frac": (t_tensor + t_hbm) / ms_max}
     if graph is not None:
         step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
-    paths = path_fractions(trace, args.steps, peaks)
+    paths = path_fractions(alone_trace, alone_steps, peaks)
+    roof_alone = None
+    g_alone = alone_trace.get("gemm_tcgen05")
+    if g_alone is not None and g_alone["total_ms"] > 0:
+        a_alone = g_alone["useful_flops"] / (g_alone["total_ms"] * 1e-3) / 1e12
+        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        roof_alone = {"bound": "tensor", "kernel": "gemm_tcgen05", "achieved": a_alone, "peak": sus,
+                      "unit": "TFLOP/s", "frac": a_alone / sus, "peak_burst": peaks["bf16_tflops"],
+                      "frac_burst": a_alone / peaks["bf16_tflops"],
+                      "launches_per_step": g_alone["launches"] / alone_steps,
+                      "method": "3 extra traced steps with the accumulation overlap off"}
+    overlap = None
+    if "accum_pool" in trace:
+        overlap = {
+            "on": True,
+            "gemm_ms_per_step": trace["gemm_tcgen05"]["total_ms"] / args.steps,
+            "gemm_ms_per_step_alone": g_alone["total_ms"] / alone_steps if g_alone else None,
+            "accum_standalone_ms_per_step": trace.get("accum_rownorm", {}).get("total_ms", 0.0) / args.steps,
+            "accum_pool_rest_ms_per_step": trace["accum_pool"]["total_ms"] / args.steps,
+            "accum_ms_per_step_alone": alone_trace.get("accum_rownorm", {}).get("total_ms", 0.0) / alone_steps,
+            "method": ("the first shape group's accumulation runs on its own; each later group's is a pool "
+                       "of rows taken by streaming warps inside the previous group's GEMM launches, the "
+                       "rest by a pool kernel")}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -581,7 +627,8 @@ def run_ours(args, rank, world, device_index):
                    "frac_of_fp16_peak": value / world / bf16_peak,
                    "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
                    "parallelism": f"{world} independent ranks (no collective on the data path)"},
-        "roofline": roof, "step_roofline": step_roof, "paths": paths, "kernels": kernels,
+        "roofline": roof, "roofline_alone": roof_alone, "overlap": overlap,
+        "step_roofline": step_roof, "paths": paths, "kernels": kernels,
         "gpu_launches": launches,
         "gpu_launches_per_step": launches / args.steps, "clocks": clock_info,
     }
@@ -787,6 +834,8 @@ def main():
                     help="16-bit type of the Gram-NS operands (the pages use fp16)")
     ap.add_argument("--max-batch", type=int, default=0,
                     help="cap the matrices per shape group (small profiling case)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="run the shape groups without the accumulation overlap (dion3_set_overlap(0))")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunk", type=int, default=16,
                     help="matrices per pipelined sub-batch in the end-to-end measurement")

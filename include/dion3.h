@@ -283,7 +283,9 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups,
  *   sel_idx_out  NULL, or a host array [ngroups] of device int32 [batch][k]
  *                buffers (entries may be NULL) that receive each matrix's
  *                selected rows, ascending.
- * With more than one group, the groups run concurrently: each on one of up to
+ * With more than one group and the accumulation overlap on (the default, see
+ * dion3_set_overlap), the groups run in order on `stream`.  With it off, the
+ * groups run concurrently: each on one of up to
  * four streams owned by the library, forked from `stream` (they wait for the
  * work already enqueued on it) and joined back into it before the call
  * returns, so later work on `stream` sees every result, and a graph captured
@@ -296,6 +298,21 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups,
 dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
                         const dion3_hparams* hp, void* ws, size_t ws_bytes,
                         int32_t* const* sel_idx_out, dion3_stream_t stream);
+
+/*
+ * Overlap of the accumulation with Newton-Schulz in dion3_step (and its lazy
+ * and NorMuon forms) with more than one shape group: on (the default), the
+ * groups run in order on `stream`, the one with the most Newton-Schulz work
+ * first; only that group's accumulation (step a's M <- M + G and row norms)
+ * runs on its own, and each later group's is handed out row by row to
+ * streaming warps inside the previous group's tensor-core GEMM launches, which
+ * move it while the tensor cores work, with a memory-bound kernel finishing
+ * the rows they did not reach.  Off, each group runs its steps in sequence,
+ * the groups on concurrent streams (see dion3_step).  Results are bit-identical
+ * either way.  Process-wide; the environment variable DION3_OVERLAP=0 sets the
+ * initial value to off.
+ */
+dion3_status dion3_set_overlap(int32_t on);
 
 /*
  * dion3_select_rows without a workspace, for callers that may not allocate

@@ -39,7 +39,7 @@ EXPORTED = (
     "dion3_step", "dion3_device_status", "dion3_gemm_f16", "dion3_trace_enable",
     "dion3_trace_collect", "dion3_select_rows_noalloc", "dion3_ns_useful_flops",
     "dion3_ns_workspace_size", "dion3_ns_batched", "dion3_step_lazy", "dion3_flush_row_scale",
-    "dion3_step_normuon", "dion3_wait_probe",
+    "dion3_step_normuon", "dion3_wait_probe", "dion3_set_overlap",
 )
 
 
@@ -116,6 +116,7 @@ _SIGS = {
                                                  ctypes.POINTER(_vp), _i32, _i32, _vp, _vp, _vp]),
     "dion3_trace_collect": (ctypes.c_int, [ctypes.POINTER(_TraceEntry), _i32, ctypes.POINTER(_i32)]),
     "dion3_wait_probe": (ctypes.c_int, [_i32, ctypes.c_int64, _vp]),
+    "dion3_set_overlap": (ctypes.c_int, [_i32]),
 }
 
 _LIB = None
@@ -445,6 +446,12 @@ def flush_row_scale(momentum: Sequence, row_scale, stream=None):
     rows, cols = momentum[0].shape
     M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momentum])
     _check(load_library().dion3_flush_row_scale(rows, cols, n, M, _ptr(row_scale), _stream(stream)))
+
+
+def set_overlap(on: bool):
+    """Overlap each shape group's accumulation with the previous group's
+    Newton-Schulz GEMMs in :func:`step` (default on; see dion3_set_overlap)."""
+    _check(load_library().dion3_set_overlap(1 if on else 0))
 
 
 def wait_probe(arrive: bool, limit_ns: int, stream=None):

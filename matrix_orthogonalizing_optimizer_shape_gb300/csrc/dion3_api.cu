@@ -11,6 +11,7 @@
 #include "internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdlib>
@@ -925,13 +926,19 @@ bool group_streams_enabled() {
 }
 
 // Whether dion3_step overlaps the accumulation of one shape group with the
-// Newton-Schulz GEMMs of another (DION3_OVERLAP, read once; default on).
+// Newton-Schulz GEMMs of another: dion3_set_overlap, initially DION3_OVERLAP
+// (default on).
+std::atomic<int> g_overlap{-1};
 bool overlap_enabled() {
-  static const bool on = [] {
-    const char* v = getenv("DION3_OVERLAP");
-    return v == nullptr || atoi(v) != 0;
-  }();
-  return on;
+  int v = g_overlap.load();
+  if (v < 0) {
+    const char* e = getenv("DION3_OVERLAP");
+    v = (e == nullptr || atoi(e) != 0) ? 1 : 0;
+    int expected = -1;
+    g_overlap.compare_exchange_strong(expected, v);
+    v = g_overlap.load();
+  }
+  return v != 0;
 }
 
 class GroupStreams {
@@ -1312,6 +1319,11 @@ dion3_status dion3_trace_collect(dion3_trace_entry* out, int32_t capacity, int32
   *count = static_cast<int32_t>(agg.size());
   for (int i = 0; i < static_cast<int>(agg.size()) && i < capacity; ++i) out[i] = agg[i];
   trace_clear_locked();
+  return ok();
+}
+
+dion3_status dion3_set_overlap(int32_t on) {
+  g_overlap.store(on != 0 ? 1 : 0);
   return ok();
 }
 

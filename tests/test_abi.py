@@ -237,3 +237,9 @@ def test_wait_probe_validation(lib):
     """dion3_wait_probe refuses a limit outside [1 us, 1 s] before any launch."""
     for bad in (0, 999, 10**9 + 1, -5):
         assert lib.dion3_wait_probe(0, bad, None) == d3.ERR_INVALID_ARG, bad
+
+
+def test_set_overlap_toggles(lib):
+    """dion3_set_overlap is a host-side switch: it launches nothing."""
+    assert lib.dion3_set_overlap(0) == d3.OK
+    assert lib.dion3_set_overlap(1) == d3.OK

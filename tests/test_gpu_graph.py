@@ -158,3 +158,29 @@ def test_overlapped_groups_match_single_group_calls(cuda_lib, lazy):
         for a, b in zip(multi[1][gi] + multi[2][gi], single[1][gi] + single[2][gi]):
             assert np.array_equal(to_host(a), to_host(b))
         assert np.array_equal(to_host(scales[0][gi]), to_host(scales[1][gi]))
+
+
+def test_overlap_on_and_off_bitwise(cuda_lib):
+    """dion3_set_overlap: the same three steps with the accumulation overlap
+    off (groups on concurrent streams, standalone accumulation) and on give
+    bit-identical selections, momenta and parameters."""
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+    runs = []
+    try:
+        for on in (False, True):
+            d3.set_overlap(on)
+            st = _build(f, seed=53)
+            ws = d3.alloc_workspace(d3.workspace_size(st[0], hp))
+            for _ in range(3):
+                d3.step(st[0], hp, ws, sel_idx_out=st[3])
+            torch.cuda.synchronize()
+            d3.device_status()
+            runs.append(st)
+    finally:
+        d3.set_overlap(True)
+    a, b = runs
+    for gi in range(len(SHAPES)):
+        assert np.array_equal(a[3][gi].cpu().numpy(), b[3][gi].cpu().numpy())
+        for x, y in zip(a[1][gi] + a[2][gi], b[1][gi] + b[2][gi]):
+            assert np.array_equal(to_host(x), to_host(y))
