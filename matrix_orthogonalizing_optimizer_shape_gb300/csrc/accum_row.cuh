@@ -45,8 +45,10 @@ __device__ __forceinline__ float accum_load_grad(const void* g, size_t i, int gd
 // Row `r` of an n x cols matrix: Mrow = M + r cols, Grow = G + r cols (or null
 // with GD = -1: norms only).  rs is the row's pending lazy-decay factor (1: none):
 // the accumulation is then M <- fp32(fp32(rs M) + G).  Returns l1 and sum of
-// squares in lane 0 (every lane holds the warp's sums).
-template <bool VEC, int GD, int U>
+// squares in lane 0 (every lane holds the warp's sums).  EVICT_M: M is read and
+// written with the evict-first policy (the gradient always is), for rows moved
+// beside a GEMM whose operands should keep L2.
+template <bool VEC, int GD, int U, bool EVICT_M = false>
 __device__ __forceinline__ void accum_row(float* __restrict__ Mrow, const void* Grow, int cols, float rs,
                                           float& l1_out, float& sq_out) {
   const int lane = threadIdx.x % 32;
@@ -64,8 +66,14 @@ __device__ __forceinline__ void accum_row(float* __restrict__ Mrow, const void* 
       for (int u = 0; u < U; ++u) {
         const int c = c0 + u * step;
         if (c < cols) {
-          const float4 x0 = *reinterpret_cast<const float4*>(Mrow + c);
-          const float4 x1 = *reinterpret_cast<const float4*>(Mrow + c + 4);
+          float4 x0, x1;
+          if constexpr (EVICT_M) {
+            x0 = __ldcs(reinterpret_cast<const float4*>(Mrow + c));
+            x1 = __ldcs(reinterpret_cast<const float4*>(Mrow + c + 4));
+          } else {
+            x0 = *reinterpret_cast<const float4*>(Mrow + c);
+            x1 = *reinterpret_cast<const float4*>(Mrow + c + 4);
+          }
           m[u][0] = x0.x; m[u][1] = x0.y; m[u][2] = x0.z; m[u][3] = x0.w;
           m[u][4] = x1.x; m[u][5] = x1.y; m[u][6] = x1.z; m[u][7] = x1.w;
           if constexpr (GD == kBF16) {
@@ -97,8 +105,15 @@ __device__ __forceinline__ void accum_row(float* __restrict__ Mrow, const void* 
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) m[u][j] = __fadd_rn(m[u][j], g[j]);
-            *reinterpret_cast<float4*>(Mrow + c) = make_float4(m[u][0], m[u][1], m[u][2], m[u][3]);
-            *reinterpret_cast<float4*>(Mrow + c + 4) = make_float4(m[u][4], m[u][5], m[u][6], m[u][7]);
+            const float4 y0 = make_float4(m[u][0], m[u][1], m[u][2], m[u][3]);
+            const float4 y1 = make_float4(m[u][4], m[u][5], m[u][6], m[u][7]);
+            if constexpr (EVICT_M) {
+              __stcs(reinterpret_cast<float4*>(Mrow + c), y0);
+              __stcs(reinterpret_cast<float4*>(Mrow + c + 4), y1);
+            } else {
+              *reinterpret_cast<float4*>(Mrow + c) = y0;
+              *reinterpret_cast<float4*>(Mrow + c + 4) = y1;
+            }
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -126,7 +141,7 @@ __device__ __forceinline__ void accum_row(float* __restrict__ Mrow, const void* 
 
 // Row `row` (= matrix b x rows + r) of an accumulation pool, processed by the
 // calling warp: the pool's bookkeeping around accum_row.
-template <int GD, int U>
+template <int GD, int U, bool EVICT_M = false>
 __device__ __forceinline__ void accum_pool_row(const AccumPool& pool, long long row) {
   const int b = static_cast<int>(row / pool.rows);
   const int r = static_cast<int>(row - static_cast<long long>(b) * pool.rows);
@@ -135,9 +150,11 @@ __device__ __forceinline__ void accum_pool_row(const AccumPool& pool, long long 
   const float rs = pool.scale != nullptr ? pool.scale[row] : 1.0f;
   float l1, sq;
   if constexpr (GD == kBF16)
-    accum_row<true, kBF16, U>(Mrow, reinterpret_cast<const uint16_t*>(pool.G[b]) + goff, pool.cols, rs, l1, sq);
+    accum_row<true, kBF16, U, EVICT_M>(Mrow, reinterpret_cast<const uint16_t*>(pool.G[b]) + goff, pool.cols, rs,
+                                       l1, sq);
   else
-    accum_row<true, kF32, U>(Mrow, reinterpret_cast<const float*>(pool.G[b]) + goff, pool.cols, rs, l1, sq);
+    accum_row<true, kF32, U, EVICT_M>(Mrow, reinterpret_cast<const float*>(pool.G[b]) + goff, pool.cols, rs, l1,
+                                      sq);
   if (threadIdx.x % 32 == 0) {
     pool.l1[row] = l1;
     pool.sq[row] = sq;

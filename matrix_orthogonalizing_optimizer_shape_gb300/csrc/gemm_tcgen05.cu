@@ -97,6 +97,7 @@ constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accum
 // ones spill at the kernel's register budget).
 constexpr int kSideUnrollBF16 = 6;
 constexpr int kSideUnrollF32 = 4;
+constexpr bool kSideEvict = true;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -746,10 +747,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (__shfl_sync(0xffffffffu, fin, 0) >= static_cast<uint32_t>(kEpiWarps)) break;
         const long long row = accum_pool_next(p.pool);
         if (row >= p.pool.total) break;
+        // Evict-first for M too: the GEMM's operand panels keep L2.
         if (p.pool.grad_dtype == kBF16)
-          accum_pool_row<kBF16, kSideUnrollBF16>(p.pool, row);
+          accum_pool_row<kBF16, kSideUnrollBF16, kSideEvict>(p.pool, row);
         else
-          accum_pool_row<kF32, kSideUnrollF32>(p.pool, row);
+          accum_pool_row<kF32, kSideUnrollF32, kSideEvict>(p.pool, row);
       }
     }
   } else {
