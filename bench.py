@@ -687,7 +687,13 @@ def run_sweep(args):
     import workloads
     d3.load_library()
     hp = d3.HParams()
-    if args.sweep_full:
+    if args.sweep_points:
+        # explicit points "s x L x batch" (Gram side, long side, matrices)
+        pts = []
+        for item in args.sweep_points.split(","):
+            s_, L_, b_ = (int(v) for v in item.lower().split("x"))
+            pts.append((s_, L_ // s_, b_))
+    elif args.sweep_full:
         pts = [(s, a, b) for s in workloads.SWEEP_S for a in workloads.SWEEP_ASPECT
                for b in workloads.SWEEP_BATCH]
     else:
@@ -824,6 +830,8 @@ def main():
     ap.add_argument("--workload", default="7b", choices=["7b", "1b", "gapped", "single", "sweep"])
     ap.add_argument("--sweep-full", action="store_true",
                     help="with --workload sweep: every (s, aspect, batch) of the sweep grid")
+    ap.add_argument("--sweep-points", default="",
+                    help="with --workload sweep: comma-separated points SxLxBATCH (e.g. 512x4096x128)")
     ap.add_argument("--f", type=float, default=0.25)
     ap.add_argument("--lazy-decay", action="store_true",
                     help="dion3_step_lazy: the selected rows' decay is carried to the next step")
