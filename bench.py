@@ -708,6 +708,11 @@ def run_sweep(args):
                 pts.append((s_, a, b))
     names = {d3.NS_GRAM: "gram", d3.NS_GRAM_DENSE: "gram_dense", d3.NS_STANDARD: "standard",
              d3.NS_STANDARD_DENSE: "standard_dense"}
+    only = set(v for v in args.sweep_variants.split(",") if v) if args.sweep_variants else None
+    if only:
+        names = {v: n for v, n in names.items() if n in only}
+        if not names:
+            raise SystemExit("--sweep-variants names none of gram, gram_dense, standard, standard_dense")
     rows = []
     s_ev = torch.cuda.current_stream()
     for (s_, a, b) in pts:
@@ -738,6 +743,8 @@ def run_sweep(args):
             del ws
         d3.device_status()
         for name, fn in (("cublas_gram", _cublas_gram_ns), ("cublas_standard", _cublas_standard_ns)):
+            if only is not None and name not in only:
+                continue
             for _ in range(2):
                 fn(X, hp)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -747,10 +754,9 @@ def run_sweep(args):
             e1.record(s_ev)
             torch.cuda.synchronize()
             row[name + "_ms"] = e0.elapsed_time(e1) / args.steps
-        row["speedup_vs_standard"] = row["standard_ms"] / row["gram_ms"]
-        row["speedup_vs_standard_dense"] = row["standard_dense_ms"] / row["gram_ms"]
-        row["speedup_vs_cublas_standard"] = row["cublas_standard_ms"] / row["gram_ms"]
-        row["speedup_vs_cublas_gram"] = row["cublas_gram_ms"] / row["gram_ms"]
+        for ref in ("standard", "standard_dense", "cublas_standard", "cublas_gram"):
+            if "gram_ms" in row and ref + "_ms" in row:
+                row["speedup_vs_" + ref] = row[ref + "_ms"] / row["gram_ms"]
         rows.append(row)
         del X, O
         torch.cuda.empty_cache()
@@ -832,6 +838,9 @@ def main():
                     help="with --workload sweep: every (s, aspect, batch) of the sweep grid")
     ap.add_argument("--sweep-points", default="",
                     help="with --workload sweep: comma-separated points SxLxBATCH (e.g. 512x4096x128)")
+    ap.add_argument("--sweep-variants", default="",
+                    help="with --workload sweep: comma-separated subset of gram, gram_dense, standard, "
+                         "standard_dense, cublas_gram, cublas_standard (default: all)")
     ap.add_argument("--f", type=float, default=0.25)
     ap.add_argument("--lazy-decay", action="store_true",
                     help="dion3_step_lazy: the selected rows' decay is carried to the next step")
