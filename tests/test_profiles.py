@@ -1,7 +1,7 @@
 """The committed DRAM-traffic record (profiles/traffic.json) that bench.py
-reports for the dominant GEMM is consistent with itself, was taken on a small
-case (one kernel, a few launches, a few GB on the device), and is used only
-while the kernel source is the one it was captured on."""
+reports for the dominant GEMM is consistent with itself, was taken on small
+captures (one kernel, a few launches, a few GB on the device each), and is used
+only while the kernel source is the one it was captured on."""
 import hashlib
 import json
 import os
@@ -28,22 +28,28 @@ def _record():
         return json.load(fh)["gemm_tcgen05"]
 
 
-def test_traffic_record_is_a_small_case_capture():
+def test_traffic_captures_are_small():
     rec = _record()
-    cmd = rec["command"]
-    assert "--clock-control none" in cmd
-    assert re.search(r"-k regex:\S*gemm", cmd), "one kernel only"
-    n = int(re.search(r"-c (\d+)", cmd).group(1))
-    assert 1 <= n <= 18, "a few launches only"
-    assert "--max-batch" in cmd, "a small case of the bench workload"
-    assert rec["device_gb"] <= 8.0
+    assert rec["captures"]
+    for cap in rec["captures"]:
+        cmd = cap["command"]
+        assert "--clock-control none" in cmd
+        assert re.search(r"-k regex:\S*gemm", cmd), "one kernel only"
+        n = int(re.search(r"-c (\d+)", cmd).group(1))
+        assert 1 <= n <= 18 and cap["launches"] == n, "a few launches only"
+        assert "--sweep-points" in cmd or "--max-batch" in cmd, "a small case, not the whole set"
+        assert cap["device_gb"] <= 8.0
+        assert "--set full" not in cmd and "--section" not in cmd
 
 
 def test_traffic_record_is_consistent():
     rec = _record()
+    caps = rec["captures"]
+    assert rec["launches"] == sum(c["launches"] for c in caps)
+    assert rec["dram_read_bytes"] == sum(c["dram_read_bytes"] for c in caps)
+    assert rec["dram_write_bytes"] == sum(c["dram_write_bytes"] for c in caps)
     per_launch = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["launches"]
-    assert abs(per_launch - rec["dram_bytes_per_launch_small"]) <= 1.0
-    assert rec["dram_bytes_per_launch"] == pytest.approx(rec["dram_bytes_per_launch_small"] * rec["scale"])
+    assert rec["dram_bytes_per_launch"] == pytest.approx(per_launch)
 
 
 def test_bench_uses_the_record_only_for_the_same_source():
