@@ -162,20 +162,6 @@ __device__ __forceinline__ void accum_pool_row(const AccumPool& pool, long long 
   }
 }
 
-// Asks L2 to fetch row `row` of the pool (its M and G) ahead of use, without
-// registers or shared memory (one lane issues it; rows are 16-byte multiples).
-__device__ __forceinline__ void accum_pool_prefetch(const AccumPool& pool, long long row) {
-  if (threadIdx.x % 32 != 0 || row >= pool.total) return;
-  const int b = static_cast<int>(row / pool.rows);
-  const int r = static_cast<int>(row - static_cast<long long>(b) * pool.rows);
-  const float* m = pool.M[b] + static_cast<size_t>(r) * pool.cols;
-  const unsigned gbytes = static_cast<unsigned>(pool.cols) * (pool.grad_dtype == kBF16 ? 2u : 4u);
-  const char* g = reinterpret_cast<const char*>(pool.G[b]) + static_cast<size_t>(r) * gbytes;
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(m), "r"(static_cast<unsigned>(pool.cols) * 4u)
-               : "memory");
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(gbytes) : "memory");
-}
-
 // Hands out the pool's next row to the calling warp (every lane gets it); a
 // value >= pool.total means the pool is exhausted.
 __device__ __forceinline__ long long accum_pool_next(const AccumPool& pool) {

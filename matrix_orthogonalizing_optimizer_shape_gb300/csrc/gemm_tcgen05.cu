@@ -98,7 +98,6 @@ constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accum
 constexpr int kSideUnrollBF16 = 6;
 constexpr int kSideUnrollF32 = 4;
 constexpr bool kSideEvict = true;
-constexpr bool kSidePrefetch = true;  // L2 prefetch of the next row before the current one
 constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -742,28 +741,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // GEMM work lasts; the rest is left for the pool kernel that follows the
     // GEMM launches ----------------
     if (p.pool.total > 0) {
-      // One row ahead: the next row is taken from the counter, and L2 asked
-      // to fetch it, before the current one is processed.  A taken row is
-      // always processed, even once the GEMM part of the CTA has finished.
-      auto gemm_done = [&]() {
+      for (;;) {
         uint32_t fin = 0;
         if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(epi_done);
-        return __shfl_sync(0xffffffffu, fin, 0) >= static_cast<uint32_t>(kEpiWarps);
-      };
-      long long row = gemm_done() ? p.pool.total : accum_pool_next(p.pool);
-      if (kSidePrefetch) accum_pool_prefetch(p.pool, row);
-      while (row < p.pool.total) {
-        long long nxt = p.pool.total;
-        if (!gemm_done()) {
-          nxt = accum_pool_next(p.pool);
-          if (kSidePrefetch) accum_pool_prefetch(p.pool, nxt);
-        }
+        if (__shfl_sync(0xffffffffu, fin, 0) >= static_cast<uint32_t>(kEpiWarps)) break;
+        const long long row = accum_pool_next(p.pool);
+        if (row >= p.pool.total) break;
         // Evict-first for M too: the GEMM's operand panels keep L2.
         if (p.pool.grad_dtype == kBF16)
           accum_pool_row<kBF16, kSideUnrollBF16, kSideEvict>(p.pool, row);
         else
           accum_pool_row<kF32, kSideUnrollF32, kSideEvict>(p.pool, row);
-        row = nxt;
       }
     }
   } else {
