@@ -217,6 +217,9 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // None of this thread's bulk groups is still reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// At most this thread's most recent bulk group may still be reading shared
+// memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Generic-proxy shared-memory writes become visible to the async proxy.
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -312,6 +315,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties registers written by an earlier tcgen05.ld to a point after the wait,
+// so no use of them is scheduled before it (no instruction is emitted).
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(v[j])::"memory");
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) core groups
@@ -479,13 +489,13 @@ __device__ __forceinline__ void prefetch_c(const GemmParams& p, int bidx, int r,
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool HAS_C>
 __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
                                              const uint4 (&cv)[4], uint32_t (&hp)[16]) {
   float f[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
-  if (p.C != nullptr && r < p.M) {
+  if (HAS_C && p.C != nullptr && r < p.M) {
     const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
     if (c_vector_ok(p, c0)) {
 #pragma unroll
@@ -592,7 +602,9 @@ __device__ __forceinline__ void diag_chunk(uint32_t buf, uint32_t sw, int lane, 
   __syncwarp();
 }
 
-template <bool BF16>
+// HAS_C: the launch has a C operand (only then are its registers set aside
+// for the C prefetch; without it the epilogue pipelines its TMEM loads).
+template <bool BF16, bool HAS_C>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAT, const __grid_constant__ CUtensorMap tmBT,
@@ -767,7 +779,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool want_t_any = sym || p.outT != nullptr;
     const bool tma_ok = (!want_n || p.tma_out) && (!want_t_any || (sym ? p.tma_out : p.tma_outT));
     const CUtensorMap* map_t = sym ? &tmOut : &tmOutT;
-    uint32_t staged = 0;  // chunks this warp has staged
+    uint32_t staged = 0;    // chunks this warp has staged
+    uint32_t fast_run = 0;  // of them, the last ones staged by the fast path (one 2 KB half each)
     uint32_t tc = 0;
     for (int u = cluster; u < p.total_units; u += nclusters, ++tc) {
       const int bidx = p.reverse ? p.batch - 1 - u / p.units_per_mat : u / p.units_per_mat;
@@ -785,18 +798,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int r = row0 + lane;
       // C of every chunk this warp will write (registers; unused entries stay
       // unread, the conditions match the chunk loop below).
-      uint4 cvs[kChunks][4];
+      uint4 cvs[HAS_C ? kChunks : 1][4];
+      if constexpr (HAS_C) {
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int c0 = bc * BN + col_lo + 32 * i;
-        if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
+        for (int i = 0; i < kChunks; ++i) {
+          const int c0 = bc * BN + col_lo + 32 * i;
+          if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
+        }
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      // Common case: every chunk of this warp is written once as a plain box
+      // (rectangular products, self-products, tiles below the diagonal of the
+      // others).  The next chunk's TMEM load is issued as soon as the current
+      // one has landed, and the warp's two 2 KB staging boxes alternate, so a
+      // chunk waits only for the bulk store of the chunk two back.
+      const bool fast = !HAS_C && tma_ok && !want_t && (!tri || P != bc) && row0 < p.M;
+      if (fast) {
+        const int nact = min(kChunks, (p.N - bc * BN - col_lo + 31) / 32);  // chunks with c0 < N
+        uint32_t va[32], vb[32];
+        auto emit = [&](int i, uint32_t (&v)[32]) {
+          const int c0 = bc * BN + col_lo + 32 * i;
+          uint32_t hp[16];
+          chunk_values<BF16, HAS_C>(p, bidx, r, c0, v, cvs[HAS_C ? i : 0], hp);
+          const uint32_t buf = my_staging + (staged & 1u) * Smem::kStageBoxBytes;
+          const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+          // The half written now was read by the store two chunks back; when the
+          // previous chunk came from the other path, its group may have read
+          // both halves, so every group must be done.
+          if (lane == 0) {
+            if (fast_run >= 1) {
+              if (staged >= 2) bulk_wait_read_1();
+            } else if (staged >= 1) {
+              bulk_wait_read_0();
+            }
+          }
+          __syncwarp();
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
+                         hp[4 * q + 2], hp[4 * q + 3]);
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmOut, buf, c0, row0, bidx);
+            bulk_commit();
+          }
+          ++staged;
+          ++fast_run;
+        };
+        if (nact > 0) {
+          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo), va);
+          tmem_ld_wait();
+          tmem_regs_ready(va);
+          if (nact > 1) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 32), vb);
+          emit(0, va);
+        }
+        if (nact > 1) {
+          tmem_ld_wait();
+          tmem_regs_ready(vb);
+          if (nact > 2) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 64), va);
+          emit(1, vb);
+        }
+        if (nact > 2) {
+          tmem_ld_wait();
+          tmem_regs_ready(va);
+          if (nact > 3) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 96), vb);
+          emit(2, va);
+        }
+        if (nact > 3) {
+          tmem_ld_wait();
+          tmem_regs_ready(vb);
+          emit(3, vb);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kChunks && !fast; ++i) {
         const int cc = col_lo + 32 * i;
         const int c0 = bc * BN + cc;
         // Warp-uniform classification of the chunk.
@@ -807,13 +886,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
         tmem_ld_wait();
         uint32_t hp[16];
-        chunk_values<BF16>(p, bidx, r, c0, v, cvs[i], hp);
+        chunk_values<BF16, HAS_C>(p, bidx, r, c0, v, cvs[HAS_C ? i : 0], hp);
         if (!tma_ok) {
           store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
           continue;
         }
         const uint32_t buf = my_staging;
         const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+        fast_run = 0;
         if (tri && row0 <= c0 + 31) {
           diag_chunk(buf, sw, lane, staged, hp);
           if (lane == 0) {
@@ -964,7 +1044,7 @@ int max_active_clusters(int dev) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Smem::kDyn;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<false>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<false, true>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
       int sms = 0;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1006,13 +1086,15 @@ bool gemm_check(const GemmDesc& g, const char** why) {
 
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
   const bool bf16 = g.elem == kBF16;
-  auto kern = bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  const bool has_c = g.C != nullptr && g.beta != 0.0f;
+  auto kern = bf16 ? (has_c ? gemm_tcgen05_kernel<true, true> : gemm_tcgen05_kernel<true, false>)
+                   : (has_c ? gemm_tcgen05_kernel<false, true> : gemm_tcgen05_kernel<false, false>);
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  static std::once_flag once[64][2];
+  static std::once_flag once[64][4];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
-  std::call_once(once[dev & 63][bf16 ? 1 : 0], [&] {
+  std::call_once(once[dev & 63][(bf16 ? 1 : 0) + (has_c ? 2 : 0)], [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1063,7 +1145,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.alpha = g.alpha;
   p.beta = g.beta;
   p.gamma = g.gamma;
-  p.C = g.C;
+  p.C = has_c ? g.C : nullptr;  // beta = 0: C is not read
   p.c_bs = g.c_bstride;
   p.ldc = g.ldc;
   p.out = g.out;
