@@ -489,13 +489,14 @@ __device__ __forceinline__ void prefetch_c(const GemmParams& p, int bidx, int r,
   }
 }
 
-template <bool BF16, bool HAS_C>
+// READ_C = false: the caller knows there is no C (the fast path).
+template <bool BF16, bool READ_C>
 __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int r, int c0, const uint32_t (&v)[32],
                                              const uint4 (&cv)[4], uint32_t (&hp)[16]) {
   float f[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) f[j] = p.alpha * __uint_as_float(v[j]);
-  if (HAS_C && p.C != nullptr && r < p.M) {
+  if (READ_C && p.C != nullptr && r < p.M) {
     const __half* crow = p.C + static_cast<long long>(bidx) * p.c_bs + static_cast<size_t>(r) * p.ldc + c0;
     if (c_vector_ok(p, c0)) {
 #pragma unroll
@@ -602,9 +603,7 @@ __device__ __forceinline__ void diag_chunk(uint32_t buf, uint32_t sw, int lane, 
   __syncwarp();
 }
 
-// HAS_C: the launch has a C operand (only then are its registers set aside
-// for the C prefetch; without it the epilogue pipelines its TMEM loads).
-template <bool BF16, bool HAS_C>
+template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAT, const __grid_constant__ CUtensorMap tmBT,
@@ -796,33 +795,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool tri = sym && !p.diag_full;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
-      // C of every chunk this warp will write (registers; unused entries stay
-      // unread, the conditions match the chunk loop below).
-      uint4 cvs[HAS_C ? kChunks : 1][4];
-      if constexpr (HAS_C) {
+      // Common case: no C, and every chunk of this warp written once as a
+      // plain box (rectangular products, self-products, tiles below the
+      // diagonal of the others).  The next chunk's TMEM load is issued as soon
+      // as the current one has landed, and the warp's two 2 KB staging boxes
+      // alternate, so a chunk waits only for the bulk store of the chunk two
+      // back.  Only the other path loads C (ahead of the accumulator), so its
+      // registers are never live beside the two TMEM buffers.
+      const bool fast = p.C == nullptr && tma_ok && !want_t && (!tri || P != bc) && row0 < p.M;
+      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      if (fast) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status))) break;
+        tc_fence_after();
+        const int nact = min(kChunks, (p.N - bc * BN - col_lo + 31) / 32);  // chunks with c0 < N
+        const uint4 no_c[4] = {};
+        uint32_t v[32];
+        if (nact > 0) {
+          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo), v);
+          tmem_ld_wait();
+          tmem_regs_ready(v);
+        }
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) {
-          const int c0 = bc * BN + col_lo + 32 * i;
-          if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
-        }
-      }
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
-      // Common case: every chunk of this warp is written once as a plain box
-      // (rectangular products, self-products, tiles below the diagonal of the
-      // others).  The next chunk's TMEM load is issued as soon as the current
-      // one has landed, and the warp's two 2 KB staging boxes alternate, so a
-      // chunk waits only for the bulk store of the chunk two back.
-      const bool fast = !HAS_C && tma_ok && !want_t && (!tri || P != bc) && row0 < p.M;
-      if (fast) {
-        const int nact = min(kChunks, (p.N - bc * BN - col_lo + 31) / 32);  // chunks with c0 < N
-        uint32_t va[32], vb[32];
-        auto emit = [&](int i, uint32_t (&v)[32]) {
+          if (i >= nact) break;
           const int c0 = bc * BN + col_lo + 32 * i;
           uint32_t hp[16];
-          chunk_values<BF16, HAS_C>(p, bidx, r, c0, v, cvs[HAS_C ? i : 0], hp);
+          chunk_values<BF16, false>(p, bidx, r, c0, v, no_c, hp);
+          // The next chunk's TMEM load runs while this one is staged and stored.
+          if (i + 1 < nact) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 32 * (i + 1)), v);
           const uint32_t buf = my_staging + (staged & 1u) * Smem::kStageBoxBytes;
           const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
           // The half written now was read by the store two chunks back; when the
@@ -848,86 +848,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           ++staged;
           ++fast_run;
-        };
-        if (nact > 0) {
-          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo), va);
-          tmem_ld_wait();
-          tmem_regs_ready(va);
-          if (nact > 1) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 32), vb);
-          emit(0, va);
+          if (i + 1 < nact) {
+            tmem_ld_wait();
+            tmem_regs_ready(v);
+          }
         }
-        if (nact > 1) {
-          tmem_ld_wait();
-          tmem_regs_ready(vb);
-          if (nact > 2) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 64), va);
-          emit(1, vb);
-        }
-        if (nact > 2) {
-          tmem_ld_wait();
-          tmem_regs_ready(va);
-          if (nact > 3) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(col_lo + 96), vb);
-          emit(2, va);
-        }
-        if (nact > 3) {
-          tmem_ld_wait();
-          tmem_regs_ready(vb);
-          emit(3, vb);
-        }
-      }
+      } else {
+        // C of every chunk this warp will write (registers; unused entries
+        // stay unread, the conditions match the chunk loop below), loaded
+        // before the accumulator is ready.
+        uint4 cvs[kChunks][4];
 #pragma unroll
-      for (int i = 0; i < kChunks && !fast; ++i) {
-        const int cc = col_lo + 32 * i;
-        const int c0 = bc * BN + cc;
-        // Warp-uniform classification of the chunk.
-        if (c0 >= p.N) break;
-        if (tri && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
-        if (row0 >= p.M) continue;            // rows out of range
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
-        tmem_ld_wait();
-        uint32_t hp[16];
-        chunk_values<BF16, HAS_C>(p, bidx, r, c0, v, cvs[HAS_C ? i : 0], hp);
-        if (!tma_ok) {
-          store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
-          continue;
+        for (int i = 0; i < kChunks; ++i) {
+          const int c0 = bc * BN + col_lo + 32 * i;
+          if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
         }
-        const uint32_t buf = my_staging;
-        const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
-        fast_run = 0;
-        if (tri && row0 <= c0 + 31) {
-          diag_chunk(buf, sw, lane, staged, hp);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status))) break;
+        tc_fence_after();
+  #pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int cc = col_lo + 32 * i;
+          const int c0 = bc * BN + cc;
+          // Warp-uniform classification of the chunk.
+          if (c0 >= p.N) break;
+          if (tri && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
+          if (row0 >= p.M) continue;            // rows out of range
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
+          tmem_ld_wait();
+          uint32_t hp[16];
+          chunk_values<BF16, true>(p, bidx, r, c0, v, cvs[i], hp);
+          if (!tma_ok) {
+            store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
+            continue;
+          }
+          const uint32_t buf = my_staging;
+          const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+          fast_run = 0;
+          if (tri && row0 <= c0 + 31) {
+            diag_chunk(buf, sw, lane, staged, hp);
+            if (lane == 0) {
+              tma_store_3d(&tmOut, buf, c0, row0, bidx);
+              bulk_commit();
+            }
+            ++staged;
+            continue;
+          }
+          // Stage the box (and its transpose) in swizzled shared memory, then
+          // one lane writes them with bulk tensor stores.
+          if (lane == 0 && staged >= 1) bulk_wait_read_0();
+          __syncwarp();
+          if (want_n) {
+  #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
+                           hp[4 * q + 2], hp[4 * q + 3]);
+          }
+          if (want_t) {
+            const uint32_t tbuf = buf + Smem::kStageBoxBytes;
+            const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
+  #pragma unroll
+            for (int j = 0; j < 32; ++j)
+              st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
+          }
+          fence_async_shared();
+          __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmOut, buf, c0, row0, bidx);
+            if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
+            if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
             bulk_commit();
           }
           ++staged;
-          continue;
         }
-        // Stage the box (and its transpose) in swizzled shared memory, then
-        // one lane writes them with bulk tensor stores.
-        if (lane == 0 && staged >= 1) bulk_wait_read_0();
-        __syncwarp();
-        if (want_n) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
-                         hp[4 * q + 2], hp[4 * q + 3]);
-        }
-        if (want_t) {
-          const uint32_t tbuf = buf + Smem::kStageBoxBytes;
-          const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
-        }
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
-          if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
-          bulk_commit();
-        }
-        ++staged;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(bar_tempty + 8 * acc, 0));
@@ -1044,7 +1036,7 @@ int max_active_clusters(int dev) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Smem::kDyn;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<false, true>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tcgen05_kernel<false>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
       int sms = 0;
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1087,14 +1079,13 @@ bool gemm_check(const GemmDesc& g, const char** why) {
 cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s) {
   const bool bf16 = g.elem == kBF16;
   const bool has_c = g.C != nullptr && g.beta != 0.0f;
-  auto kern = bf16 ? (has_c ? gemm_tcgen05_kernel<true, true> : gemm_tcgen05_kernel<true, false>)
-                   : (has_c ? gemm_tcgen05_kernel<false, true> : gemm_tcgen05_kernel<false, false>);
+  auto kern = bf16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  static std::once_flag once[64][4];
+  static std::once_flag once[64][2];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
-  std::call_once(once[dev & 63][(bf16 ? 1 : 0) + (has_c ? 2 : 0)], [&] {
+  std::call_once(once[dev & 63][bf16 ? 1 : 0], [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kDyn);
   });
   if (attr_err != cudaSuccess) return attr_err;
