@@ -795,14 +795,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool tri = sym && !p.diag_full;
       const int row0 = bi * BM + quad * 32;
       const int r = row0 + lane;
-      // Common case: no C, and every chunk of this warp written once as a
-      // plain box (rectangular products, self-products, tiles below the
-      // diagonal of the others).  The next chunk's TMEM load is issued as soon
-      // as the current one has landed, and the warp's two 2 KB staging boxes
-      // alternate, so a chunk waits only for the bulk store of the chunk two
-      // back.  Only the other path loads C (ahead of the accumulator), so its
-      // registers are never live beside the two TMEM buffers.
-      const bool fast = p.C == nullptr && tma_ok && !want_t && (!tri || P != bc) && row0 < p.M;
+      // Rectangular products without C (Q Y at the restart and at the end):
+      // every chunk of this warp is written once as a plain box, so the next
+      // chunk's TMEM load can run while the current one is staged and stored,
+      // and the warp's two 2 KB staging boxes alternate, a chunk waiting only
+      // for the bulk store of the chunk two back.  (Measured per role: these
+      // products 8-10 % faster at s = 512.  Taken for the off-diagonal tiles
+      // of symmetric products too, it made those 2-4 % slower: switching to
+      // and from the mirrored path of their diagonal tiles waits for every
+      // store.)  Only the other path loads C, so its registers are never live
+      // here.
+      const bool fast = p.mode == kRect && p.C == nullptr && tma_ok && !want_t && row0 < p.M;
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(quad * 32) << 16);
       if (fast) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status))) break;
