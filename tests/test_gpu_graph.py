@@ -184,3 +184,41 @@ def test_overlap_on_and_off_bitwise(cuda_lib):
         assert np.array_equal(a[3][gi].cpu().numpy(), b[3][gi].cpu().numpy())
         for x, y in zip(a[1][gi] + a[2][gi], b[1][gi] + b[2][gi]):
             assert np.array_equal(to_host(x), to_host(y))
+
+
+def test_overlap_with_groups_that_cannot_be_pooled(cuda_lib):
+    """The overlapped schedule with groups whose accumulation cannot be a pool
+    (130 matrices, more than a pool holds; 70 columns, not a multiple of 8):
+    they accumulate with the standalone kernel in their turn.  Against the same
+    groups stepped one call at a time: bit-identical over two steps."""
+    shapes = [(64, 64, 130, "bf16"), (40, 70, 3, "f32"), (300, 200, 2, "bf16")]
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.9, lr=0.01)
+
+    def build():
+        groups, sels = [], []
+        for gi, (n, m, batch, pd) in enumerate(shapes):
+            M = [to_dev(workloads.gapped_momentum(n, m, seed=900 + 1000 * gi + b)) for b in range(batch)]
+            W = [to_dev(workloads.gaussian((n, m), 0.02, seed=901 + 1000 * gi + b, dtype=pd), pd)
+                 for b in range(batch)]
+            G = [to_dev(workloads.gaussian((n, m), 0.01, seed=902 + 1000 * gi + b, dtype="bf16"), "bf16")
+                 for b in range(batch)]
+            groups.append(d3.Group(params=W, grads=G, momentum=M))
+            sels.append(torch.empty((batch, d3.num_selected(f, n)), dtype=torch.int32, device="cuda"))
+        return groups, sels
+
+    multi, sel_m = build()
+    single, sel_s = build()
+    ws_m = d3.alloc_workspace(d3.workspace_size(multi, hp))
+    ws_s = [d3.alloc_workspace(d3.workspace_size([g], hp)) for g in single]
+    for _ in range(2):
+        d3.step(multi, hp, ws_m, sel_idx_out=sel_m)
+        for gi, g in enumerate(single):
+            d3.step([g], hp, ws_s[gi], sel_idx_out=[sel_s[gi]])
+    torch.cuda.synchronize()
+    d3.device_status()
+    for gi in range(len(shapes)):
+        assert np.array_equal(sel_m[gi].cpu().numpy(), sel_s[gi].cpu().numpy())
+        for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
+                        list(single[gi].params) + list(single[gi].momentum)):
+            assert np.array_equal(to_host(a), to_host(b))
