@@ -82,6 +82,24 @@ def workload_groups(name: str, max_batch: int = 0):
     raise SystemExit(f"unknown workload {name}")
 
 
+def workload_config(args, groups, desc):
+    """The `config` object of the JSON line: the workload only, the same for our
+    arm and the reference arm."""
+    nbytes = {"bf16": 2, "f32": 4}
+    resident = sum(r * c * b * (nbytes[pd] + nbytes[gd] + 4) for (r, c, b, pd, gd) in groups)
+    return {"workload": f"{desc}, f={args.f}", "f": args.f,
+            "matrices": sum(g[2] for g in groups),
+            "params_per_gpu": sum(g[0] * g[1] * g[2] for g in groups),
+            "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
+            "ns": f"Gram NS T=5 restart@3, {args.ns_dtype} operands",
+            "momentum_decay": "lazy (dion3_step_lazy)" if args.lazy_decay else "eager (dion3_step)",
+            "normuon": "per-neuron normalisation (dion3_step_normuon, NorMuon reading)" if args.normuon else None,
+            "l2": (f"inputs larger than L2 ({resident / 1e9:.1f} GB of W, G, M resident in HBM against 129 MB)"
+                   if resident > 129e6 else
+                   f"inputs ({resident / 1e6:.1f} MB) smaller than L2 and not flushed between steps "
+                   "(a small parity workload, not the default line)")}
+
+
 def useful_flops_total(groups, f, hp_kwargs, d3):
     hp = d3.HParams(f=f, **hp_kwargs)
     tot = 0.0
@@ -620,17 +638,10 @@ def run_ours(args, rank, world, device_index):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.ns_dtype, "data": "synthetic",
-        "config": {"workload": f"{desc}, f={args.f}", "f": args.f,
-                   "matrices": sum(g[2] for g in groups), "params_per_gpu": sum(g[0] * g[1] * g[2] for g in groups),
-                   "param_dtype": groups[0][3], "grad_dtype": groups[0][4], "momentum_dtype": "f32",
-                   "ns": f"Gram NS T=5 restart@3, {args.ns_dtype} operands, fp32 accumulate",
-                   "momentum_decay": "lazy (dion3_step_lazy)" if args.lazy_decay else "eager (dion3_step)",
-                   "normuon": (f"per-neuron normalisation (dion3_step_normuon, NorMuon reading): beta2={nm.beta2}, "
-                               f"eps={nm.eps}, rms={nm.rms}") if args.normuon else None,
-                   "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
-                   "frac_of_fp16_peak": value / world / bf16_peak,
-                   "l2": "inputs larger than L2 (W, G, M resident in HBM, >> 129 MB)",
-                   "parallelism": f"{world} independent ranks (no collective on the data path)"},
+        "config": workload_config(args, groups, desc),
+        "useful_tflop_per_step_per_gpu": flops_rank / 1e12,
+        "frac_of_fp16_peak": value / world / bf16_peak,
+        "parallelism": f"{world} independent ranks (no collective on the data path)",
         "roofline": roof, "roofline_alone": roof_alone, "overlap": overlap,
         "step_roofline": step_roof, "paths": paths, "kernels": kernels,
         "gpu_launches": launches,
@@ -798,12 +809,14 @@ def run_reference(args):
             "W": workloads.gaussian((r, c), 0.02, seed=1, dtype=pd),
             "M": workloads.gaussian((r, c), 0.05, seed=2),
             "G": workloads.gaussian((r, c), 0.01, seed=3, dtype=gd)})
-    # Each step runs the oracle on ONE matrix, rotating through the shape groups;
-    # the step's full-set estimate combines the latest per-matrix time of every
-    # group, scaled by the group sizes.  W >= 3 warm-up steps cover every group
-    # of the model-shaped sets before the timed steps.
+    # Each step runs the oracle on ONE matrix, rotating through the shape groups.
+    # `value` is the oracle's useful throughput on this workload: the full set's
+    # FLOPs over the full set's time as the sampled per-matrix times put it
+    # (each group's latest time times its size).  `ms_per_step` is the wall time
+    # a sampled step actually took; the full-set estimate is reported beside it.
+    # W >= 3 warm-up steps cover every group of the model-shaped sets first.
     group_t = [None] * len(groups)
-    times = []
+    est, walls = [], []
     for it in range(args.warmup + args.steps):
         g = it % len(groups)
         smp = samples[g]
@@ -811,20 +824,25 @@ def run_reference(args):
         t0 = time.perf_counter()
         W, M, _, _ = oracle_step(smp["W"], smp["M"], smp["G"], f=args.f, mu=0.95, lr=0.02,
                                  param_dtype=pd)
-        group_t[g] = time.perf_counter() - t0
+        dt = time.perf_counter() - t0
+        group_t[g] = dt
         smp["W"], smp["M"] = W.astype(np.float32), M
         if it >= args.warmup:
-            times.append(sum(t * grp[2] for t, grp in zip(group_t, groups)))
-    ms = 1e3 * sum(times) / len(times)
-    value = flops / (ms * 1e-3) / 1e12
-    sample = ("float64 oracle on one matrix per step, rotating through the shape groups; each "
-              "step's estimate sums the latest per-matrix time of every group times its size "
-              f"({', '.join(f'{r}x{c} x{b}' for (r, c, b, _, _) in groups)})")
+            est.append(sum(t * grp[2] for t, grp in zip(group_t, groups)))
+            walls.append(dt)
+    full_ms = 1e3 * sum(est) / len(est)
+    value = flops / (full_ms * 1e-3) / 1e12
+    ms = 1e3 * sum(walls) / len(walls)
+    sample = ("float64 oracle on one matrix per step, rotating through the shape groups "
+              f"({', '.join(f'{r}x{c} x{b}' for (r, c, b, _, _) in groups)}); value = the full set's useful "
+              "FLOPs over the sum of each group's latest per-matrix time times its size")
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_full_set_est": full_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{desc}, f={args.f}", "f": args.f},
+            "config": workload_config(args, groups, desc),
+            "useful_tflop_per_step_per_gpu": flops / 1e12,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
