@@ -46,7 +46,7 @@
 // 128 r .. 128 r + 127 of A and rows 128 r .. 128 r + 127 of the B panel in its
 // own shared memory, and receives rows 128 r .. of the result in its own TMEM.
 // A ring slot therefore holds 32 KB per CTA (its A tile and its half of B), so
-// the 192 KB ring is 6 slots deep.  10 warps per CTA:
+// the 192 KB ring is 6 slots deep.  12 warps per CTA:
 //   warp 0         TMA producer (both CTAs): the whole warp runs the loop and
 //                  waits, one elected lane fills the CTA's own slot and
 //                  signals the even CTA's "full" barrier (cta_group::2 copy);
@@ -61,9 +61,14 @@
 //                  the accumulator is ready): tcgen05.ld, alpha/beta/gamma,
 //                  then the 32 x 32 box
 //                  (and its transpose) staged in swizzled shared memory and
-//                  written with bulk tensor stores (chunks on the diagonal of
-//                  a symmetric result are written element by element); then
-//                  they tell the even CTA that the accumulator is free.
+//                  written with bulk tensor stores (a chunk on the diagonal
+//                  of a symmetric result as one symmetric box); then they
+//                  tell the even CTA that the accumulator is free;
+//   warps 10, 11   streaming warps (and warp 1 of the odd CTA, which issues
+//                  no MMAs): when the launch carries an accumulation pool
+//                  (GemmDesc::pool), rows of another shape group's step a0
+//                  taken from the pool's counter while this CTA's GEMM work
+//                  lasts; otherwise they go straight to the final barrier.
 // Running the producer and MMA loops on whole warps keeps their loop state
 // warp-uniform; a single-lane loop (`if (lane == 0)`) measured 3-18 % slower
 // once its body branched between copy shapes.
