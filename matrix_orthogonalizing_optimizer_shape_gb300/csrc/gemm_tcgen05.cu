@@ -103,6 +103,11 @@ constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accum
 constexpr int kSideUnrollBF16 = 6;
 constexpr int kSideUnrollF32 = 4;
 constexpr bool kSideEvict = true;
+// The streaming warps take no new row once this CTA's TMA producer has issued
+// its last copy (the MMAs and epilogues of the last tiles still cover the row
+// being moved), rather than once its epilogue warps have finished: a long row
+// then holds back the CTA's exit, and the next launch, less.
+constexpr bool kSideStopAtProducer = true;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -628,9 +633,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bar_tempty + 2 * 8;
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kStagingBytes + Smem::kBarBytes);
-  // Epilogue warps of this CTA that have finished (the streaming warps stop
-  // taking rows once all have).
+  // Epilogue warps of this CTA that have finished, and whether its TMA
+  // producer has issued its last copy (the streaming warps stop taking rows at
+  // one of the two, see kSideStopAtProducer).
   uint32_t* epi_done = tmem_slot + 1;
+  uint32_t* prod_done = tmem_slot + 2;
 
   // The next kernel on the stream may be scheduled once every CTA of this one
   // has started (programmatic dependent launch).
@@ -654,6 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_drain, 1);
     fence_mbar_init();
     *epi_done = 0u;
+    *prod_done = 0u;
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -711,6 +719,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
+      if (lane == 0) *reinterpret_cast<volatile uint32_t*>(prod_done) = 1u;
       // Wait (bounded) until every copy issued into the ring has landed, so no
       // copy is in flight when the pair exits (the even CTA's barriers count
       // the bytes of both CTAs).
@@ -759,8 +768,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.pool.total > 0) {
       for (;;) {
         uint32_t fin = 0;
-        if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(epi_done);
-        if (__shfl_sync(0xffffffffu, fin, 0) >= static_cast<uint32_t>(kEpiWarps)) break;
+        if (lane == 0)
+          fin = kSideStopAtProducer ? *reinterpret_cast<volatile uint32_t*>(prod_done)
+                                    : (*reinterpret_cast<volatile uint32_t*>(epi_done) >=
+                                       static_cast<uint32_t>(kEpiWarps));
+        if (__shfl_sync(0xffffffffu, fin, 0) != 0u) break;
         const long long row = accum_pool_next(p.pool);
         if (row >= p.pool.total) break;
         // Evict-first for M too: the GEMM's operand panels keep L2.
