@@ -67,8 +67,9 @@
 //   warps 10, 11   streaming warps (and warp 1 of the odd CTA, which issues
 //                  no MMAs): when the launch carries an accumulation pool
 //                  (GemmDesc::pool), rows of another shape group's step a0
-//                  taken from the pool's counter while this CTA's GEMM work
-//                  lasts; otherwise they go straight to the final barrier.
+//                  taken from the pool's counter until this CTA's producer has
+//                  issued its last copy; otherwise they go straight to the
+//                  final barrier.
 // Running the producer and MMA loops on whole warps keeps their loop state
 // warp-uniform; a single-lane loop (`if (lane == 0)`) measured 3-18 % slower
 // once its body branched between copy shapes.
@@ -103,11 +104,6 @@ constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accum
 constexpr int kSideUnrollBF16 = 6;
 constexpr int kSideUnrollF32 = 4;
 constexpr bool kSideEvict = true;
-// The streaming warps take no new row once this CTA's TMA producer has issued
-// its last copy (the MMAs and epilogues of the last tiles still cover the row
-// being moved), rather than once its epilogue warps have finished: a long row
-// then holds back the CTA's exit, and the next launch, less.
-constexpr bool kSideStopAtProducer = true;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -633,11 +629,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bar_tempty + 2 * 8;
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + Smem::kRingBytes + Smem::kStagingBytes + Smem::kBarBytes);
-  // Epilogue warps of this CTA that have finished, and whether its TMA
-  // producer has issued its last copy (the streaming warps stop taking rows at
-  // one of the two, see kSideStopAtProducer).
-  uint32_t* epi_done = tmem_slot + 1;
-  uint32_t* prod_done = tmem_slot + 2;
+  // Whether this CTA's TMA producer has issued its last copy: the streaming
+  // warps take no new row after that.  The MMAs and epilogues of the last
+  // tiles still cover the row being moved, and the CTA's exit (and with it the
+  // next launch) waits less for a long row than if they stopped once the
+  // epilogue warps had finished (measured 0.1-0.2 ms per step faster).
+  uint32_t* prod_done = tmem_slot + 1;
 
   // The next kernel on the stream may be scheduled once every CTA of this one
   // has started (programmatic dependent launch).
@@ -660,7 +657,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_drain, 1);
     fence_mbar_init();
-    *epi_done = 0u;
     *prod_done = 0u;
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
@@ -762,16 +758,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= 2 + kEpiWarps || warp == 1) {
     // ---------------- streaming warps (and warp 1 of the odd CTA, which
     // issues no MMAs): rows of another shape group's step a0 (M <- M + G and
-    // row norms), taken from the pool's counter one at a time while this CTA's
-    // GEMM work lasts; the rest is left for the pool kernel that follows the
-    // GEMM launches ----------------
+    // row norms), taken from the pool's counter one at a time until this CTA's
+    // producer has issued its last copy; the rest is left for the pool kernel
+    // that follows the GEMM launches ----------------
     if (p.pool.total > 0) {
       for (;;) {
         uint32_t fin = 0;
-        if (lane == 0)
-          fin = kSideStopAtProducer ? *reinterpret_cast<volatile uint32_t*>(prod_done)
-                                    : (*reinterpret_cast<volatile uint32_t*>(epi_done) >=
-                                       static_cast<uint32_t>(kEpiWarps));
+        if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(prod_done);
         if (__shfl_sync(0xffffffffu, fin, 0) != 0u) break;
         const long long row = accum_pool_next(p.pool);
         if (row >= p.pool.total) break;
@@ -946,10 +939,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // Every bulk store has finished before the CTA (and its shared memory)
     // goes away.
-    if (lane == 0) {
-      bulk_wait_all();
-      atomicAdd(epi_done, 1u);
-    }
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
   tc_fence_before();
