@@ -610,8 +610,10 @@ def run_ours(args, rank, world, device_index):
         step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
     paths = path_fractions(alone_trace, alone_steps, peaks)
     roof_alone = None
-    g_alone = alone_trace.get("gemm_tcgen05")
-    if g_alone is not None and g_alone["total_ms"] > 0:
+    # All GEMM entries together (one entry, or one per role with DION3_TRACE_DETAIL).
+    g_alone = {k: sum(v[k] for v in alone_trace.values() if v["useful_flops"] > 0)
+               for k in ("total_ms", "useful_flops", "launches")}
+    if g_alone["total_ms"] > 0:
         a_alone = g_alone["useful_flops"] / (g_alone["total_ms"] * 1e-3) / 1e12
         sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
         roof_alone = {"bound": "tensor", "kernel": "gemm_tcgen05", "achieved": a_alone, "peak": sus,
@@ -623,10 +625,11 @@ def run_ours(args, rank, world, device_index):
         roof_alone["traffic"] = tr_alone["dram_bytes_per_launch"] if tr_alone else None
     overlap = None
     if "accum_pool" in trace:
+        gemm_ms = sum(v["total_ms"] for v in trace.values() if v["useful_flops"] > 0)
         overlap = {
             "on": True,
-            "gemm_ms_per_step": trace["gemm_tcgen05"]["total_ms"] / args.steps,
-            "gemm_ms_per_step_alone": g_alone["total_ms"] / alone_steps if g_alone else None,
+            "gemm_ms_per_step": gemm_ms / args.steps,
+            "gemm_ms_per_step_alone": g_alone["total_ms"] / alone_steps,
             "accum_standalone_ms_per_step": trace.get("accum_rownorm", {}).get("total_ms", 0.0) / args.steps,
             "accum_pool_rest_ms_per_step": trace["accum_pool"]["total_ms"] / args.steps,
             "accum_ms_per_step_alone": alone_trace.get("accum_rownorm", {}).get("total_ms", 0.0) / alone_steps,
