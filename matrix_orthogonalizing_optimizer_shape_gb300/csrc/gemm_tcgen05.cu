@@ -526,7 +526,9 @@ __device__ __forceinline__ void chunk_values(const GemmParams& p, int bidx, int 
         if (c0 + j < p.N) f[j] = fmaf(p.beta, unpack1<BF16>(__half_as_ushort(crow[j])), f[j]);
     }
   }
-  if (p.gamma != 0.0f) {
+  // gamma I meets only the chunk whose columns are the warp's rows (both
+  // start at a multiple of 32).
+  if (p.gamma != 0.0f && c0 == (r & ~31)) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (r == c0 + j) f[j] += p.gamma;
@@ -833,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           tmem_regs_ready(v);
         }
-#pragma unroll
+#pragma unroll 1
         for (int i = 0; i < kChunks; ++i) {
           if (i >= nact) break;
           const int c0 = bc * BN + col_lo + 32 * i;
@@ -872,71 +874,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // C of every chunk this warp will write (registers; unused entries
-        // stay unread, the conditions match the chunk loop below), loaded
-        // before the accumulator is ready.
-        uint4 cvs[kChunks][4];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
+        // Chunks this warp writes: inside the matrix, rows in range, and not
+        // wholly above the diagonal of a triangle-only result.
+        auto writes = [&](int i) {
           const int c0 = bc * BN + col_lo + 32 * i;
-          if (c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M) prefetch_c(p, bidx, r, c0, cvs[i]);
-        }
+          return c0 < p.N && !(tri && row0 + 31 < c0) && row0 < p.M;
+        };
+        // C of the first chunk is loaded before the accumulator is ready, and
+        // each chunk loads the next one's while it is processed.  The loop
+        // stays rolled: one copy of the chunk code (TMEM load, epilogue
+        // values, staging of the box, its transpose or a symmetric diagonal
+        // box, bulk stores) instead of four.
+        uint4 cv[4] = {}, cv_next[4] = {};
+        if (writes(0)) prefetch_c(p, bidx, r, bc * BN + col_lo, cv);
         if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, aph, p.status))) break;
         tc_fence_after();
-  #pragma unroll
+#pragma unroll 1
         for (int i = 0; i < kChunks; ++i) {
           const int cc = col_lo + 32 * i;
           const int c0 = bc * BN + cc;
-          // Warp-uniform classification of the chunk.
           if (c0 >= p.N) break;
-          if (tri && row0 + 31 < c0) continue;  // wholly above the diagonal: nothing to write
-          if (row0 >= p.M) continue;            // rows out of range
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
-          tmem_ld_wait();
-          uint32_t hp[16];
-          chunk_values<BF16, true>(p, bidx, r, c0, v, cvs[i], hp);
-          if (!tma_ok) {
-            store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
-            continue;
-          }
-          const uint32_t buf = my_staging;
-          const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
-          fast_run = 0;
-          if (tri && row0 <= c0 + 31) {
-            diag_chunk(buf, sw, lane, staged, hp);
-            if (lane == 0) {
-              tma_store_3d(&tmOut, buf, c0, row0, bidx);
-              bulk_commit();
+          if (i + 1 < kChunks && writes(i + 1)) prefetch_c(p, bidx, r, c0 + 32, cv_next);
+          if (writes(i)) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(cc), v);
+            tmem_ld_wait();
+            uint32_t hp[16];
+            chunk_values<BF16, true>(p, bidx, r, c0, v, cv, hp);
+            const uint32_t buf = my_staging;
+            const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+            if (!tma_ok) {
+              store_chunk_scalar(p, bidx, r, c0, row0, hp, want_t);
+            } else if (tri && row0 <= c0 + 31) {
+              fast_run = 0;
+              diag_chunk(buf, sw, lane, staged, hp);
+              if (lane == 0) {
+                tma_store_3d(&tmOut, buf, c0, row0, bidx);
+                bulk_commit();
+              }
+              ++staged;
+            } else {
+              fast_run = 0;
+              // Stage the box (and its transpose) in swizzled shared memory,
+              // then one lane writes them with bulk tensor stores.
+              if (lane == 0 && staged >= 1) bulk_wait_read_0();
+              __syncwarp();
+              if (want_n) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
+                               hp[4 * q + 2], hp[4 * q + 3]);
+              }
+              if (want_t) {
+                const uint32_t tbuf = buf + Smem::kStageBoxBytes;
+                const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
+              }
+              fence_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
+                if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
+                bulk_commit();
+              }
+              ++staged;
             }
-            ++staged;
-            continue;
           }
-          // Stage the box (and its transpose) in swizzled shared memory, then
-          // one lane writes them with bulk tensor stores.
-          if (lane == 0 && staged >= 1) bulk_wait_read_0();
-          __syncwarp();
-          if (want_n) {
-  #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(buf + lane * 64 + ((static_cast<uint32_t>(q) ^ sw) << 4), hp[4 * q], hp[4 * q + 1],
-                           hp[4 * q + 2], hp[4 * q + 3]);
-          }
-          if (want_t) {
-            const uint32_t tbuf = buf + Smem::kStageBoxBytes;
-            const uint32_t lo = static_cast<uint32_t>(lane & 7) << 1, hi = static_cast<uint32_t>(lane >> 3);
-  #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              st_shared_u16(tbuf + j * 64 + (((hi ^ ((j >> 1) & 3)) << 4) | lo), half_bits(hp, j));
-          }
-          fence_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            if (want_n) tma_store_3d(&tmOut, buf, c0, row0, bidx);
-            if (want_t) tma_store_3d(map_t, buf + Smem::kStageBoxBytes, row0, c0, bidx);
-            bulk_commit();
-          }
-          ++staged;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cv[q] = cv_next[q];
         }
       }
       tc_fence_before();
