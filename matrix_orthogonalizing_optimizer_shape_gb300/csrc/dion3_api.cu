@@ -325,6 +325,18 @@ cudaError_t traced_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
   const double bytes = static_cast<double>(a.batch) * a.k * a.cols * (2.0 + 2.0 * pb);
   return traced("scatter_update", 0.0, bytes, s, [&] { return launch_scatter(a, vec, s); });
 }
+// The rest of a scatter pool.  Its trace entry carries the algorithmic bytes
+// of every deferred update in the pool, part of which the streaming warps of
+// the GEMM launches before it have written.
+cudaError_t traced_scatter_pool(const ScatterPool& p, cudaStream_t s) {
+  double bytes = 0.0;
+  for (int i = 0; i < p.nseg; ++i) {
+    const ScatterSeg& g = p.seg[i];
+    const double pb = g.param_dtype == kBF16 ? 2.0 : 4.0;
+    bytes += static_cast<double>(g.batch) * g.k * g.cols * (2.0 + 2.0 * pb);
+  }
+  return traced("scatter_pool", 0.0, bytes, s, [&] { return launch_scatter_pool(p, s); });
+}
 cudaError_t traced_normuon_rows(const NormRowsArgs& a, bool vec, cudaStream_t s) {
   // O read once; per row: the index, v read and written, d and rowc written.
   const double bytes = static_cast<double>(a.batch) * a.k * (2.0 * a.m + 4.0 + 8.0 + 8.0);
@@ -370,7 +382,8 @@ struct NsOut {
 };
 
 dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& out, unsigned* st,
-                         cudaStream_t stream, bool dense = false, const AccumPool* pool = nullptr) {
+                         cudaStream_t stream, bool dense = false, const AccumPool* pool = nullptr,
+                         const ScatterPool* spool = nullptr) {
   TraceChain chain("gemm_tcgen05", stream);
   // Symmetric product of two s x s matrices (or, with xi >= 0, the SYRK
   // R = Y Y^T from X[xi]: Y itself when wide, given as its transpose X = Y^T
@@ -407,10 +420,11 @@ dion3_status run_gram_ns(const NsPlan& p, const dion3_hparams& hp, const NsOut& 
   auto launch = [&](const GemmDesc& g0) -> dion3_status {
     GemmDesc g = g0;
     g.elem = hp.ns_dtype == DION3_BF16 ? kBF16 : kF16;
-    // Every launch of the run lends its streaming warps to the pool (limiting
+    // Every launch of the run lends its streaming warps to the pools (limiting
     // that to the launches with a long K, whose epilogue warps are idle more
     // of the time, measured no better).
     g.pool = pool;
+    g.spool = spool;
     g.reverse = reverse;
     reverse = !reverse;
     const char* why = nullptr;
@@ -622,6 +636,7 @@ struct GroupPlan {
   float* nm_d;     // per-neuron normalisation: row factors [batch][k]
   float* nm_rowc;  // and the rows' d^2 q [batch][k]
   unsigned long long* pool_next;  // row counter when this group's accumulation is pooled
+  unsigned long long* spool_next; // row counter of the scatter pool riding on this group's launches
   NsPlan ns;
 };
 
@@ -640,6 +655,7 @@ void plan_group(Carver& c, const dion3_group& g, float f, GroupPlan& gp) {
   gp.nm_d = c.take<float>(static_cast<long long>(g.batch) * gp.k);
   gp.nm_rowc = c.take<float>(static_cast<long long>(g.batch) * gp.k);
   gp.pool_next = c.take<unsigned long long>(1);
+  gp.spool_next = c.take<unsigned long long>(1);
   plan_ns(c, gp.k, gp.m, gp.batch, gp.ns);
 }
 
@@ -1079,10 +1095,11 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
     }
   };
   // Top-k, gather/normalise (+ decay of the selected momentum rows), Gram-NS
-  // (its GEMM launches lending their streaming warps to `pool`), the
-  // per-neuron normalisation if asked, and the scatter update of group gi.
-  auto select_orthogonalise_update = [&](int gi, cudaStream_t s, const AccumPool* pool,
-                                         int pool_gi) -> dion3_status {
+  // (its GEMM launches lending their streaming warps to `pool`, then to
+  // `spool`), the per-neuron normalisation if asked, and the scatter update of
+  // group gi unless it is deferred into a later group's scatter pool.
+  auto select_orthogonalise_update = [&](int gi, cudaStream_t s, const AccumPool* pool, int pool_gi,
+                                         const ScatterPool* spool, bool defer) -> dion3_status {
     const dion3_group& g = groups[gi];
     const GroupPlan& gp = plans[gi];
     int32_t* idx = sel_of(gi);
@@ -1111,14 +1128,22 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       e = cudaMemsetAsync(pool->next, 0, sizeof(unsigned long long), s);
       if (e != cudaSuccess) return cuda_fail(e, "pool counter reset");
     }
+    if (spool != nullptr) {
+      e = cudaMemsetAsync(spool->next, 0, sizeof(unsigned long long), s);
+      if (e != cudaSuccess) return cuda_fail(e, "scatter pool counter reset");
+    }
     NsOut out{gp.O, gp.o_bs, gp.ld_o};
-    dion3_status rc2 = run_gram_ns(gp.ns, *hp, out, st, s, false, pool);
+    dion3_status rc2 = run_gram_ns(gp.ns, *hp, out, st, s, false, pool, spool);
     if (rc2 != DION3_OK) return rc2;
     if (pool != nullptr) {
       // Rows of the pool the streaming warps did not reach.
       if ((e = traced_accum_pool(*pool, s)) != cudaSuccess) return cuda_fail(e, "accum_pool launch");
     } else if (pool_gi >= 0) {
       if ((rc2 = accumulate(pool_gi, s)) != DION3_OK) return rc2;
+    }
+    if (spool != nullptr) {
+      // Deferred updates the streaming warps did not reach.
+      if ((e = traced_scatter_pool(*spool, s)) != cudaSuccess) return cuda_fail(e, "scatter_pool launch");
     }
     if (nm != nullptr) {
       // Per-neuron normalisation of the k orthogonalised rows (v of the
@@ -1136,7 +1161,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       if ((e = traced_normuon_scale(sc, s)) != cudaSuccess) return cuda_fail(e, "normuon scale launch");
     }
     // (c) scatter update of the selected parameter rows.
-    for (int b0 = 0; b0 < g.batch; b0 += kMaxBatchPerLaunch) {
+    for (int b0 = 0; b0 < g.batch && !defer; b0 += kMaxBatchPerLaunch) {
       const int nb = std::min(kMaxBatchPerLaunch, g.batch - b0);
       ScatterArgs sa{};
       sa.rows = g.rows; sa.cols = g.cols; sa.k = gp.k; sa.batch = nb; sa.param_dtype = g.param_dtype;
@@ -1166,6 +1191,42 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       work[gi] = schedule_flops(plans[gi].k, groups[gi].cols, *hp) * groups[gi].batch;
     }
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work[x] > work[y]; });
+    // The last group's GEMM launches have no accumulation to carry; they carry
+    // the scatter updates of up to kScatterSegMax earlier groups instead (the
+    // ones nearest to it; groups with per-neuron normalisation, ragged rows or
+    // more than kPoolMax matrices keep their own scatter launches).  Each such
+    // group's O and selected indices stay in its part of the workspace until
+    // then.
+    std::vector<char> deferred(ngroups, 0);
+    ScatterPool spool;
+    {
+      int nd = 0;
+      for (int i = ngroups - 2; i >= 0 && nd < kScatterSegMax; --i) {
+        const int gi = order[i];
+        if (nm == nullptr && groups[gi].cols % 8 == 0 && groups[gi].batch <= kPoolMax) {
+          deferred[gi] = 1;
+          ++nd;
+        }
+      }
+      for (int i = 0; i + 1 < ngroups; ++i) {
+        const int gi = order[i];
+        if (!deferred[gi]) continue;
+        const dion3_group& g = groups[gi];
+        const GroupPlan& gp = plans[gi];
+        ScatterSeg& sg = spool.seg[spool.nseg++];
+        sg.start = spool.total;
+        sg.rows = g.rows; sg.cols = g.cols; sg.k = gp.k; sg.batch = g.batch;
+        sg.param_dtype = g.param_dtype == DION3_BF16 ? kBF16 : kF32;
+        sg.o_bf16 = hp->ns_dtype == DION3_BF16;
+        sg.idx = sel_of(gi);
+        sg.O = gp.O; sg.o_bstride = gp.o_bs; sg.ld_o = gp.ld_o;
+        sg.lr = lr_eff;
+        for (int b = 0; b < g.batch; ++b) sg.W[b] = g.params[b];
+        spool.total += static_cast<long long>(g.batch) * gp.k;
+      }
+      spool.next = plans[order[ngroups - 1]].spool_next;
+      spool.status = st;
+    }
     if ((rc = accumulate(order[0], s0)) != DION3_OK) return rc;
     for (int i = 0; i < ngroups; ++i) {
       const int gi = order[i];
@@ -1173,7 +1234,10 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
       AccumPool pool;
       const bool pooled = nx >= 0 && poolable(nx);
       if (pooled) make_pool(nx, pool);
-      if ((rc = select_orthogonalise_update(gi, s0, pooled ? &pool : nullptr, nx)) != DION3_OK) return rc;
+      const bool carries = nx < 0 && spool.total > 0;
+      if ((rc = select_orthogonalise_update(gi, s0, pooled ? &pool : nullptr, nx, carries ? &spool : nullptr,
+                                            deferred[gi] != 0)) != DION3_OK)
+        return rc;
     }
     return ok();
   }
@@ -1187,7 +1251,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
   for (int gi = 0; gi < ngroups; ++gi) {
     cudaStream_t s = fork.stream(gi);
     if ((rc = accumulate(gi, s)) != DION3_OK) return rc;
-    if ((rc = select_orthogonalise_update(gi, s, nullptr, -1)) != DION3_OK) return rc;
+    if ((rc = select_orthogonalise_update(gi, s, nullptr, -1, nullptr, false)) != DION3_OK) return rc;
   }
   if ((fe = fork.end()) != cudaSuccess) return cuda_fail(fe, "group stream join");
   return ok();

@@ -66,10 +66,11 @@
 //                  tell the even CTA that the accumulator is free;
 //   warps 10, 11   streaming warps (and warp 1 of the odd CTA, which issues
 //                  no MMAs): when the launch carries an accumulation pool
-//                  (GemmDesc::pool), rows of another shape group's step a0
-//                  taken from the pool's counter until this CTA's producer has
-//                  issued its last copy; otherwise they go straight to the
-//                  final barrier.
+//                  (GemmDesc::pool), rows of another shape group's step a0,
+//                  then, when it carries a scatter pool (GemmDesc::spool),
+//                  rows of deferred step a7 updates, each taken from its
+//                  pool's counter until this CTA's producer has issued its
+//                  last copy; otherwise they go straight to the final barrier.
 // Running the producer and MMA loops on whole warps keeps their loop state
 // warp-uniform; a single-lane loop (`if (lane == 0)`) measured 3-18 % slower
 // once its body branched between copy shapes.
@@ -79,6 +80,7 @@
 // barrier before freeing TMEM, and TMEM is freed on every path.
 #include "accum_row.cuh"
 #include "internal.h"
+#include "scatter_row.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -104,6 +106,7 @@ constexpr int kSideWarps = 2;  // streaming warps: rows of another group's accum
 constexpr int kSideUnrollBF16 = 6;
 constexpr int kSideUnrollF32 = 4;
 constexpr bool kSideEvict = true;
+constexpr int kSideUnrollScatter = 4;  // bf16 parameters; half of it for fp32 ones
 constexpr int kThreads = 32 * (2 + kEpiWarps + kSideWarps);
 constexpr int kTmemCols = 512; // two 256-column accumulators
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
@@ -125,6 +128,7 @@ struct GemmParams {
   int diag_full;             // out_half: diagonal super-tiles written whole, as computed (no mirror)
   unsigned* status;
   AccumPool pool;            // rows for the streaming warps (total 0: none)
+  ScatterPool spool;         // then these (total 0: none)
 };
 
 // ---------------------------------------------------------------------------
@@ -765,14 +769,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= 2 + kEpiWarps || warp == 1) {
     // ---------------- streaming warps (and warp 1 of the odd CTA, which
     // issues no MMAs): rows of another shape group's step a0 (M <- M + G and
-    // row norms), taken from the pool's counter one at a time until this CTA's
-    // producer has issued its last copy; the rest is left for the pool kernel
-    // that follows the GEMM launches ----------------
+    // row norms), then rows of deferred step a7 updates, taken from the
+    // pools' counters one at a time until this CTA's producer has issued its
+    // last copy; the rest is left for the pool kernels that follow the GEMM
+    // launches ----------------
+    auto producer_done = [&]() {
+      uint32_t fin = 0;
+      if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(prod_done);
+      return __shfl_sync(0xffffffffu, fin, 0) != 0u;
+    };
+    bool stop = false;
     if (p.pool.total > 0) {
       for (;;) {
-        uint32_t fin = 0;
-        if (lane == 0) fin = *reinterpret_cast<volatile uint32_t*>(prod_done);
-        if (__shfl_sync(0xffffffffu, fin, 0) != 0u) break;
+        if (producer_done()) {
+          stop = true;
+          break;
+        }
         const long long row = accum_pool_next(p.pool);
         if (row >= p.pool.total) break;
         // Evict-first for M too: the GEMM's operand panels keep L2.
@@ -780,6 +792,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           accum_pool_row<kBF16, kSideUnrollBF16, kSideEvict>(p.pool, row);
         else
           accum_pool_row<kF32, kSideUnrollF32, kSideEvict>(p.pool, row);
+      }
+    }
+    if (!stop && p.spool.total > 0) {
+      for (;;) {
+        if (producer_done()) break;
+        const long long row = scatter_pool_next(p.spool);
+        if (row >= p.spool.total) break;
+        scatter_pool_row<kSideUnrollScatter>(p.spool, row);
       }
     }
   } else {
@@ -1185,6 +1205,7 @@ cudaError_t launch_gemm(const GemmDesc& g, unsigned* dev_status, cudaStream_t s)
   p.diag_full = (g.mode == kSymLower && g.out_half && self && c_sym && diag_full_enabled()) ? 1 : 0;
   p.status = dev_status;
   if (g.pool != nullptr) p.pool = *g.pool;
+  if (g.spool != nullptr) p.spool = *g.spool;
 
   const int clusters = static_cast<int>(std::min<long long>(total, max_active_clusters(dev)));
   const int grid = 2 * clusters;

@@ -91,6 +91,32 @@ struct AccumPool {
 // The rest of a pool: every row the counter has not handed out yet.
 cudaError_t launch_accum_pool(const AccumPool& p, cudaStream_t s);
 
+// Step a7 of shape groups whose update is deferred (their O and selected
+// indices stay in the workspace) as one pool of rows, one segment per group,
+// handed out by a device counter: to the streaming warps of the GEMM launches
+// that run meanwhile (GemmDesc::spool), then to launch_scatter_pool for what is
+// left.  Every row is written exactly once, with the arithmetic of the scatter
+// kernel (vector path: cols a multiple of 8; no per-row factors).
+constexpr int kScatterSegMax = 2;  // deferred groups per pool
+struct ScatterSeg {
+  long long start = 0;               // the segment's first row of the pool
+  int rows = 0, cols = 0, k = 0, batch = 0;
+  int param_dtype = kBF16;           // kF32 or kBF16
+  bool o_bf16 = false;               // O holds bf16 (else fp16)
+  const int32_t* idx = nullptr;      // [batch][k]
+  const __half* O = nullptr; long long o_bstride = 0; int ld_o = 0;   // [batch][k][ld_o]
+  float lr = 0.f;
+  void* W[kPoolMax];
+};
+struct ScatterPool {
+  long long total = 0;                 // rows over all segments; 0: no pool
+  int nseg = 0;
+  unsigned long long* next = nullptr;  // rows handed out so far; zero before the pool's first user
+  unsigned* status = nullptr;          // device status word (kDevCheck on a bad index)
+  ScatterSeg seg[kScatterSegMax];
+};
+cudaError_t launch_scatter_pool(const ScatterPool& p, cudaStream_t s);
+
 // a1: top-k rows by l1 (ties to the lower index), indices ascending, and
 // fro2 = sum of sq over the selected rows.
 struct TopkArgs {
@@ -213,8 +239,10 @@ struct GemmDesc {
   // B stored [batch][K][N] (ldb >= N); read as MN-major tiles.
   bool a_tr = false, b_tr = false;
   // Optional: rows of another shape group's step a0 for the launch's
-  // streaming warps to take while the tensor cores work (null: none).
+  // streaming warps to take while the tensor cores work (null: none), and
+  // rows of deferred step a7 updates, taken once `pool` is exhausted.
   const AccumPool* pool = nullptr;
+  const ScatterPool* spool = nullptr;
 };
 
 // Host-side checks of a descriptor (alignment and pitch rules of the TMA

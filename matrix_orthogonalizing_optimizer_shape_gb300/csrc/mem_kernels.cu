@@ -8,6 +8,7 @@
 // rows are updated; error feedback decays only the chosen momentum rows by mu.
 #include "accum_row.cuh"
 #include "internal.h"
+#include "scatter_row.cuh"
 
 #include <cuda_bf16.h>
 
@@ -22,15 +23,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-  }
 }
 
 // 16-bit operand elements of the Gram-NS path: fp16, or bf16 when BF16.
@@ -484,47 +476,29 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __grid_constant__ Sc
   const __half* O = a.O + static_cast<long long>(b) * a.o_bstride + static_cast<size_t>(i) * a.ld_o;
   const int cols = a.cols;
   const float nlr = NORM ? -(a.lr * a.row_factor[static_cast<size_t>(b) * a.k + i]) : -a.lr;
-  if constexpr (PD == kBF16) {
+  if constexpr (VEC) {
+    void* W = PD == kBF16 ? static_cast<void*>(reinterpret_cast<__nv_bfloat16*>(a.W[b]) + static_cast<size_t>(row) * cols)
+                          : static_cast<void*>(reinterpret_cast<float*>(a.W[b]) + static_cast<size_t>(row) * cols);
+    scatter_row<PD, BF16>(W, O, cols, nlr);
+  } else if constexpr (PD == kBF16) {
     __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(a.W[b]) + static_cast<size_t>(row) * cols;
-    if constexpr (VEC) {
-      for (int c = lane * 8; c < cols; c += kWarp * 8) {
-        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
-        const uint4 w = *reinterpret_cast<const uint4*>(W + c);
-        float wf[8];
-        bf16x8_to_f32(w, wf);
-        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-        uint32_t outw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 of = e16x2_to_f32<BF16>(ow[j]);
-          const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(nlr, of.x, wf[2 * j]), fmaf(nlr, of.y, wf[2 * j + 1]));
-          outw[j] = *reinterpret_cast<const uint32_t*>(&r);
-        }
-        *reinterpret_cast<uint4*>(W + c) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-      }
-    } else {
-      for (int c = lane; c < cols; c += kWarp)
-        W[c] = __float2bfloat16_rn(fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), __bfloat162float(W[c])));
-    }
+    for (int c = lane; c < cols; c += kWarp)
+      W[c] = __float2bfloat16_rn(fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), __bfloat162float(W[c])));
   } else {
     float* W = reinterpret_cast<float*>(a.W[b]) + static_cast<size_t>(row) * cols;
-    if constexpr (VEC) {
-      for (int c = lane * 8; c < cols; c += kWarp * 8) {
-        const uint4 o = *reinterpret_cast<const uint4*>(O + c);
-        float4 w0 = *reinterpret_cast<const float4*>(W + c);
-        float4 w1 = *reinterpret_cast<const float4*>(W + c + 4);
-        const float2 o0 = e16x2_to_f32<BF16>(o.x), o1 = e16x2_to_f32<BF16>(o.y);
-        const float2 o2 = e16x2_to_f32<BF16>(o.z), o3 = e16x2_to_f32<BF16>(o.w);
-        w0.x = fmaf(nlr, o0.x, w0.x); w0.y = fmaf(nlr, o0.y, w0.y);
-        w0.z = fmaf(nlr, o1.x, w0.z); w0.w = fmaf(nlr, o1.y, w0.w);
-        w1.x = fmaf(nlr, o2.x, w1.x); w1.y = fmaf(nlr, o2.y, w1.y);
-        w1.z = fmaf(nlr, o3.x, w1.z); w1.w = fmaf(nlr, o3.y, w1.w);
-        *reinterpret_cast<float4*>(W + c) = w0;
-        *reinterpret_cast<float4*>(W + c + 4) = w1;
-      }
-    } else {
-      for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), W[c]);
-    }
+    for (int c = lane; c < cols; c += kWarp) W[c] = fmaf(nlr, e16_to_f32<BF16>(__half_as_ushort(O[c])), W[c]);
+  }
+}
+
+// The rest of a scatter pool: warps take rows from the pool's counter until
+// it is exhausted.
+__global__ void __launch_bounds__(256) scatter_pool_kernel(const __grid_constant__ ScatterPool p) {
+  pdl_trigger();
+  pdl_wait();
+  for (;;) {
+    const long long row = scatter_pool_next(p);
+    if (row >= p.total) break;
+    scatter_pool_row<1>(p, row);
   }
 }
 
@@ -714,6 +688,16 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool vec, cudaStream_t s) {
               : (norm ? scatter_kernel<kF32, false, false, true> : scatter_kernel<kF32, false, false>);
   }
   return launch_kernel(false, k, dim3(ceil_div(total, 8)), dim3(256), 0, s, a);
+}
+
+cudaError_t launch_scatter_pool(const ScatterPool& p, cudaStream_t s) {
+  int sms = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long want = std::max<long long>(1, ceil_div(p.total, 8));
+  const int grid = static_cast<int>(std::min<long long>(static_cast<long long>(sms) * 8, want));
+  return launch_kernel(false, scatter_pool_kernel, dim3(grid), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_normuon_rows(const NormRowsArgs& a, bool vec, cudaStream_t s) {

@@ -117,13 +117,20 @@ def test_trace_counts_launches_and_work(cuda_lib):
         want += d3.useful_flops(k, m, hp) * batch
     assert gemm["useful_flops"] == pytest.approx(want, rel=1e-9)
     assert gemm["total_ms"] > 0
-    for name in ("topk_select", "gather_normalize", "scatter_update"):
+    for name in ("topk_select", "gather_normalize"):
         assert trace[name]["launches"] == len(SHAPES), name
         assert trace[name]["total_ms"] > 0
     # Each group's accumulation: standalone, or (overlapped with the previous
     # group's Newton-Schulz GEMMs) a pool finished by one pool kernel.
     acc = sum(trace[n]["launches"] for n in ("accum_rownorm", "accum_pool") if n in trace)
     assert acc == len(SHAPES)
+    # Each group's scatter update: its own launch, or (the two groups before
+    # the last, whose rows all take the vector path here) rows of the scatter
+    # pool carried by the last group's GEMM launches and finished by one pool
+    # kernel.
+    assert trace["scatter_update"]["launches"] == len(SHAPES) - 2
+    assert trace["scatter_pool"]["launches"] == 1
+    assert trace["scatter_pool"]["total_ms"] > 0
 
 
 @pytest.mark.parametrize("lazy", [False, True])
@@ -217,6 +224,53 @@ def test_overlap_with_groups_that_cannot_be_pooled(cuda_lib):
             d3.step([g], hp, ws_s[gi], sel_idx_out=[sel_s[gi]])
     torch.cuda.synchronize()
     d3.device_status()
+    for gi in range(len(shapes)):
+        assert np.array_equal(sel_m[gi].cpu().numpy(), sel_s[gi].cpu().numpy())
+        for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
+                        list(single[gi].params) + list(single[gi].momentum)):
+            assert np.array_equal(to_host(a), to_host(b))
+
+
+def test_deferred_scatter_with_more_groups_than_the_pool_holds(cuda_lib):
+    """Four groups: the last group's GEMM launches carry the scatter updates
+    of the two groups before it (a scatter pool of two segments, fp32 and bf16
+    parameters), the first group keeps its own scatter launch.  Against the
+    same groups stepped one call at a time: bit-identical selections, momenta
+    and parameters over two steps, and the launch counts of that schedule."""
+    shapes = [(256, 128, 4, "bf16"), (128, 256, 3, "f32"), (96, 72, 5, "bf16"), (200, 136, 2, "f32")]
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.9, lr=0.01)
+
+    def build():
+        groups, sels = [], []
+        for gi, (n, m, batch, pd) in enumerate(shapes):
+            M = [to_dev(workloads.gapped_momentum(n, m, seed=700 + 1000 * gi + b)) for b in range(batch)]
+            W = [to_dev(workloads.gaussian((n, m), 0.02, seed=701 + 1000 * gi + b, dtype=pd), pd)
+                 for b in range(batch)]
+            G = [to_dev(workloads.gaussian((n, m), 0.01, seed=702 + 1000 * gi + b, dtype="bf16"), "bf16")
+                 for b in range(batch)]
+            groups.append(d3.Group(params=W, grads=G, momentum=M))
+            sels.append(torch.empty((batch, d3.num_selected(f, n)), dtype=torch.int32, device="cuda"))
+        return groups, sels
+
+    multi, sel_m = build()
+    single, sel_s = build()
+    ws_m = d3.alloc_workspace(d3.workspace_size(multi, hp))
+    ws_s = [d3.alloc_workspace(d3.workspace_size([g], hp)) for g in single]
+    d3.trace_enable(True)
+    try:
+        for _ in range(2):
+            d3.step(multi, hp, ws_m, sel_idx_out=sel_m)
+            trace = d3.trace_collect()
+            for gi, g in enumerate(single):
+                d3.step([g], hp, ws_s[gi], sel_idx_out=[sel_s[gi]])
+            d3.trace_collect()
+    finally:
+        d3.trace_enable(False)
+    torch.cuda.synchronize()
+    d3.device_status()
+    assert trace["scatter_update"]["launches"] == 2
+    assert trace["scatter_pool"]["launches"] == 1
     for gi in range(len(shapes)):
         assert np.array_equal(sel_m[gi].cpu().numpy(), sel_s[gi].cpu().numpy())
         for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
