@@ -568,9 +568,10 @@ def run_ours(args, rank, world, device_index):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "peak_kind": f"hbm copy ({peak_src})"}
     roof["frac"] = achieved / peak
-    if "accum_pool" in trace:
+    if "accum_pool" in trace or "scatter_pool" in trace:
         roof["note"] = ("the GEMM launches also carry the streaming warps that move part of the next "
-                        "shape group's accumulation (see overlap); roofline_alone is the GEMM on its own")
+                        "shape group's accumulation and of earlier groups' scatter updates (see overlap); "
+                        "roofline_alone is the GEMM on its own")
     if roof["bound"] == "tensor":
         # the same rate against the burst figure (a kernel timed on its own)
         roof["peak_burst"] = peaks["bf16_tflops"]
@@ -580,7 +581,8 @@ def run_ours(args, rank, world, device_index):
     tr = traffic_record(dom_name)
     # The record is the GEMM on its own; launches that also carry accumulation
     # rows move more, so their traffic is left open.
-    roof["traffic"] = tr["dram_bytes_per_launch"] if tr and "accum_pool" not in trace else None
+    side = "accum_pool" in trace or "scatter_pool" in trace
+    roof["traffic"] = tr["dram_bytes_per_launch"] if tr and not side else None
     kernels = {}
     tot_ms = sum(v["total_ms"] for v in trace.values())
     for name, v in sorted(trace.items(), key=lambda kv: -kv[1]["total_ms"]):
@@ -588,10 +590,12 @@ def run_ours(args, rank, world, device_index):
               "ms_per_step": v["total_ms"] / args.steps, "share": v["total_ms"] / tot_ms}
         if v["useful_flops"] > 0:
             kv["tflops"] = v["useful_flops"] / (v["total_ms"] * 1e-3) / 1e12
-        if v["algo_bytes"] > 0 and v["useful_flops"] == 0 and name != "accum_pool":
+        if v["algo_bytes"] > 0 and v["useful_flops"] == 0 and name not in ("accum_pool", "scatter_pool"):
             kv["gbs"] = v["algo_bytes"] / (v["total_ms"] * 1e-3) / 1e9
         if name == "accum_pool":
             kv["note"] = "the rows of the pooled accumulations that the GEMM launches' streaming warps left"
+        if name == "scatter_pool":
+            kv["note"] = "the rows of the deferred scatter updates that the GEMM launches' streaming warps left"
         kernels[name] = kv
 
     value = job_tflops(flops_rank, world, ms_max)
@@ -633,9 +637,13 @@ def run_ours(args, rank, world, device_index):
             "accum_standalone_ms_per_step": trace.get("accum_rownorm", {}).get("total_ms", 0.0) / args.steps,
             "accum_pool_rest_ms_per_step": trace["accum_pool"]["total_ms"] / args.steps,
             "accum_ms_per_step_alone": alone_trace.get("accum_rownorm", {}).get("total_ms", 0.0) / alone_steps,
+            "scatter_standalone_ms_per_step": trace.get("scatter_update", {}).get("total_ms", 0.0) / args.steps,
+            "scatter_pool_rest_ms_per_step": trace.get("scatter_pool", {}).get("total_ms", 0.0) / args.steps,
+            "scatter_ms_per_step_alone": alone_trace.get("scatter_update", {}).get("total_ms", 0.0) / alone_steps,
             "method": ("the first shape group's accumulation runs on its own; each later group's is a pool "
                        "of rows taken by streaming warps inside the previous group's GEMM launches, the "
-                       "rest by a pool kernel")}
+                       "rest by a pool kernel; the last group's GEMM launches carry the scatter updates "
+                       "of up to two earlier groups the same way")}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
