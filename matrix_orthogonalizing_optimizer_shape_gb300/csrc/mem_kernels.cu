@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
       a.scale_out[static_cast<size_t>(b) * a.n + row] = a.mu;
     float* src = a.M[b] + static_cast<size_t>(row) * a.m;
     if constexpr (VEC) {
-      constexpr int U = 2;  // steps of loads in flight per lane
+      constexpr int U = 4;  // steps of loads in flight per lane
       const int step = kWarp * 8;
       for (int c0 = cbeg + lane * 8; c0 < m; c0 += step * U) {
         float4 x[U][2];
