@@ -231,15 +231,18 @@ def test_overlap_with_groups_that_cannot_be_pooled(cuda_lib):
             assert np.array_equal(to_host(a), to_host(b))
 
 
-def test_deferred_scatter_with_more_groups_than_the_pool_holds(cuda_lib):
+@pytest.mark.parametrize("ns_dtype", ["f16", "bf16"])
+def test_deferred_scatter_with_more_groups_than_the_pool_holds(cuda_lib, ns_dtype):
     """Four groups: the last group's GEMM launches carry the scatter updates
-    of the two groups before it (a scatter pool of two segments, fp32 and bf16
-    parameters), the first group keeps its own scatter launch.  Against the
-    same groups stepped one call at a time: bit-identical selections, momenta
-    and parameters over two steps, and the launch counts of that schedule."""
-    shapes = [(256, 128, 4, "bf16"), (128, 256, 3, "f32"), (96, 72, 5, "bf16"), (200, 136, 2, "f32")]
+    of the two groups before it (a scatter pool of two segments), the first
+    group keeps its own scatter launch; O in fp16 or bf16, parameters in fp32
+    and bf16 (the deferred pair is, in Newton-Schulz order, a bf16 and an fp32
+    group).  Against the same groups stepped one call at a time:
+    bit-identical selections, momenta and parameters over two steps, and the
+    launch counts of that schedule."""
+    shapes = [(256, 128, 4, "bf16"), (128, 256, 3, "bf16"), (96, 72, 5, "bf16"), (200, 136, 2, "f32")]
     f = 0.5
-    hp = d3.HParams(f=f, mu=0.9, lr=0.01)
+    hp = d3.HParams(f=f, mu=0.9, lr=0.01, ns_dtype=d3.BF16 if ns_dtype == "bf16" else d3.F16)
 
     def build():
         groups, sels = [], []
