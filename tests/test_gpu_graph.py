@@ -279,3 +279,48 @@ def test_deferred_scatter_with_more_groups_than_the_pool_holds(cuda_lib, ns_dtyp
         for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
                         list(single[gi].params) + list(single[gi].momentum)):
             assert np.array_equal(to_host(a), to_host(b))
+
+
+def test_deferred_scatter_carried_by_long_launches_bitwise(cuda_lib):
+    """Groups of 8 to 32 matrices up to 2048 x 2048 at f = 1/2: the last
+    group (32 matrices of 1024 x 2048, the least Newton-Schulz work) has
+    rectangular and SYRK launches long enough for their streaming warps to
+    take most of the deferred scatter rows of the two groups before it (the
+    rest by the scatter pool kernel).  Two steps with the overlap on (deferred updates)
+    and off (every group its own scatter launch) give bit-identical
+    selections, momenta and parameters."""
+    shapes = [(2048, 2048, 8, torch.bfloat16), (2048, 1024, 8, torch.float32), (1024, 2048, 32, torch.bfloat16)]
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+
+    def build():
+        groups, sels = [], []
+        for gi, (n, m, batch, pd) in enumerate(shapes):
+            M = [workloads.device_gaussian_(torch.empty((n, m), device="cuda"), 1.0, 5000 + 100 * gi + b)
+                 for b in range(batch)]
+            W = [workloads.device_gaussian_(torch.empty((n, m), device="cuda"), 0.02, 6000 + 100 * gi + b).to(pd)
+                 for b in range(batch)]
+            G = [workloads.device_gaussian_(torch.empty((n, m), device="cuda"), 0.01, 7000 + 100 * gi + b)
+                 .to(torch.bfloat16) for b in range(batch)]
+            groups.append(d3.Group(params=W, grads=G, momentum=M))
+            sels.append(torch.empty((batch, d3.num_selected(f, n)), dtype=torch.int32, device="cuda"))
+        return groups, sels
+
+    runs = []
+    try:
+        for on in (True, False):
+            d3.set_overlap(on)
+            groups, sels = build()
+            ws = d3.alloc_workspace(d3.workspace_size(groups, hp))
+            for _ in range(2):
+                d3.step(groups, hp, ws, sel_idx_out=sels)
+            torch.cuda.synchronize()
+            d3.device_status()
+            runs.append((groups, sels))
+    finally:
+        d3.set_overlap(True)
+    (ga, sa), (gb, sb) = runs
+    for gi in range(len(shapes)):
+        assert torch.equal(sa[gi], sb[gi])
+        for x, y in zip(list(ga[gi].params) + list(ga[gi].momentum), list(gb[gi].params) + list(gb[gi].momentum)):
+            assert torch.equal(x, y)
