@@ -57,13 +57,14 @@
 //                  both CTAs with multicast commits;
 //   warps 2..9     epilogue (both CTAs): two warps per TMEM lane quadrant
 //                  (warp % 4), each taking half of the 256 columns, 32 at a
-//                  time (C, when given, is loaded for the whole tile before
-//                  the accumulator is ready): tcgen05.ld, alpha/beta/gamma,
-//                  then the 32 x 32 box
-//                  (and its transpose) staged in swizzled shared memory and
+//                  time in a rolled loop (C, when given, loaded one chunk
+//                  ahead, the first chunk's before the accumulator is ready):
+//                  tcgen05.ld, alpha/beta/gamma, then the 32 x 32 box (and
+//                  its transpose) staged in swizzled shared memory and
 //                  written with bulk tensor stores (a chunk on the diagonal
-//                  of a symmetric result as one symmetric box); then they
-//                  tell the even CTA that the accumulator is free;
+//                  of a symmetric result as one symmetric box); then one
+//                  CTA-scope arrive per thread tells the even CTA that the
+//                  accumulator is free;
 //   warps 10, 11   streaming warps (and warp 1 of the odd CTA, which issues
 //                  no MMAs): when the launch carries an accumulation pool
 //                  (GemmDesc::pool), rows of another shape group's step a0,
