@@ -324,3 +324,55 @@ def test_deferred_scatter_carried_by_long_launches_bitwise(cuda_lib):
         assert torch.equal(sa[gi], sb[gi])
         for x, y in zip(list(ga[gi].params) + list(ga[gi].momentum), list(gb[gi].params) + list(gb[gi].momentum)):
             assert torch.equal(x, y)
+
+
+def test_all_zero_group_with_deferred_update_leaves_parameters_unchanged(cuda_lib):
+    """A group whose momentum and gradients are all zero, stepped with two
+    other groups: its update is deferred into the last group's launches (it
+    has the most Newton-Schulz work, so it runs first), X = 0 / (0 + eps) and
+    O are zero, and W - lr O leaves every parameter bit-identical; the
+    momentum stays zero and the other groups match single-group calls."""
+    shapes = [(512, 512, 4, "bf16"), (256, 384, 3, "f32"), (128, 256, 2, "bf16")]
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+
+    def build(zero):
+        groups, sels = [], []
+        for gi, (n, m, batch, pd) in enumerate(shapes):
+            if gi == 0 and zero:
+                M = [torch.zeros((n, m), device="cuda") for _ in range(batch)]
+                G = [torch.zeros((n, m), device="cuda", dtype=torch.bfloat16) for _ in range(batch)]
+            else:
+                M = [to_dev(workloads.gapped_momentum(n, m, seed=300 + 10 * gi + b)) for b in range(batch)]
+                G = [to_dev(workloads.gaussian((n, m), 0.01, seed=301 + 10 * gi + b, dtype="bf16"), "bf16")
+                     for b in range(batch)]
+            W = [to_dev(workloads.gaussian((n, m), 0.02, seed=302 + 10 * gi + b, dtype=pd), pd) for b in range(batch)]
+            groups.append(d3.Group(params=W, grads=G, momentum=M))
+            sels.append(torch.empty((batch, d3.num_selected(f, n)), dtype=torch.int32, device="cuda"))
+        return groups, sels
+
+    multi, sel_m = build(True)
+    w0 = [w.clone() for w in multi[0].params]
+    single, sel_s = build(True)
+    ws_m = d3.alloc_workspace(d3.workspace_size(multi, hp))
+    ws_s = [d3.alloc_workspace(d3.workspace_size([g], hp)) for g in single]
+    d3.trace_enable(True)
+    try:
+        d3.step(multi, hp, ws_m, sel_idx_out=sel_m)
+        trace = d3.trace_collect()
+    finally:
+        d3.trace_enable(False)
+    for gi, g in enumerate(single):
+        d3.step([g], hp, ws_s[gi], sel_idx_out=[sel_s[gi]])
+    torch.cuda.synchronize()
+    d3.device_status()
+    assert trace["scatter_pool"]["launches"] == 1
+    for a, b in zip(multi[0].params, w0):
+        assert torch.equal(a, b)
+    for m in multi[0].momentum:
+        assert not torch.any(m)
+    for gi in range(1, len(shapes)):
+        assert np.array_equal(sel_m[gi].cpu().numpy(), sel_s[gi].cpu().numpy())
+        for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
+                        list(single[gi].params) + list(single[gi].momentum)):
+            assert np.array_equal(to_host(a), to_host(b))
