@@ -287,8 +287,8 @@ dion3_status dion3_workspace_size(const dion3_group* groups, int32_t ngroups,
  * dion3_set_overlap), the groups run in order on `stream`: each group's
  * momentum accumulation runs inside the previous group's Newton-Schulz
  * launches, and the parameter updates of up to two groups before the last
- * (without per-neuron normalisation, columns a multiple of 8, at most 128
- * matrices) inside the last group's; every result is written by the time the
+ * (columns a multiple of 8, at most 128 matrices) inside the last group's;
+ * every result is written by the time the
  * call's work on `stream` completes, as without the overlap.  With it off, the
  * groups run concurrently: each on one of up to
  * four streams owned by the library, forked from `stream` (they wait for the

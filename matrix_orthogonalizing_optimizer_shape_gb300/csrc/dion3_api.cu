@@ -1193,17 +1193,17 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work[x] > work[y]; });
     // The last group's GEMM launches have no accumulation to carry; they carry
     // the scatter updates of up to kScatterSegMax earlier groups instead (the
-    // ones nearest to it; groups with per-neuron normalisation, ragged rows or
-    // more than kPoolMax matrices keep their own scatter launches).  Each such
-    // group's O and selected indices stay in its part of the workspace until
-    // then.
+    // ones nearest to it; groups with ragged rows or more than kPoolMax
+    // matrices keep their own scatter launches).  Each such group's O,
+    // selected indices and per-neuron row factors stay in its part of the
+    // workspace until then.
     std::vector<char> deferred(ngroups, 0);
     ScatterPool spool;
     {
       int nd = 0;
       for (int i = ngroups - 2; i >= 0 && nd < kScatterSegMax; --i) {
         const int gi = order[i];
-        if (nm == nullptr && groups[gi].cols % 8 == 0 && groups[gi].batch <= kPoolMax) {
+        if (groups[gi].cols % 8 == 0 && groups[gi].batch <= kPoolMax) {
           deferred[gi] = 1;
           ++nd;
         }
@@ -1221,6 +1221,7 @@ dion3_status step_impl(const dion3_group* groups, int32_t ngroups, const dion3_h
         sg.idx = sel_of(gi);
         sg.O = gp.O; sg.o_bstride = gp.o_bs; sg.ld_o = gp.ld_o;
         sg.lr = lr_eff;
+        sg.row_factor = nm != nullptr ? gp.nm_d : nullptr;
         for (int b = 0; b < g.batch; ++b) sg.W[b] = g.params[b];
         spool.total += static_cast<long long>(g.batch) * gp.k;
       }

@@ -96,7 +96,7 @@ cudaError_t launch_accum_pool(const AccumPool& p, cudaStream_t s);
 // handed out by a device counter: to the streaming warps of the GEMM launches
 // that run meanwhile (GemmDesc::spool), then to launch_scatter_pool for what is
 // left.  Every row is written exactly once, with the arithmetic of the scatter
-// kernel (vector path: cols a multiple of 8; no per-row factors).
+// kernel (vector path: cols a multiple of 8).
 constexpr int kScatterSegMax = 2;  // deferred groups per pool
 struct ScatterSeg {
   long long start = 0;               // the segment's first row of the pool
@@ -106,6 +106,7 @@ struct ScatterSeg {
   const int32_t* idx = nullptr;      // [batch][k]
   const __half* O = nullptr; long long o_bstride = 0; int ld_o = 0;   // [batch][k][ld_o]
   float lr = 0.f;
+  const float* row_factor = nullptr; // [batch][k]: row i's lr is lr * row_factor[b][i] (null: lr)
   void* W[kPoolMax];
 };
 struct ScatterPool {

@@ -101,7 +101,8 @@ __device__ __forceinline__ void scatter_pool_row(const ScatterPool& p, long long
     return;
   }
   const __half* O = g.O + static_cast<long long>(b) * g.o_bstride + static_cast<size_t>(i) * g.ld_o;
-  const float nlr = -g.lr;
+  // The scatter kernel's expression, so a deferred normalised row gets the same bits.
+  const float nlr = g.row_factor != nullptr ? -(g.lr * g.row_factor[static_cast<size_t>(b) * g.k + i]) : -g.lr;
   if (g.param_dtype == kBF16) {
     void* W = reinterpret_cast<__nv_bfloat16*>(g.W[b]) + static_cast<size_t>(r) * g.cols;
     if (g.o_bf16) scatter_row<kBF16, true, U>(W, O, g.cols, nlr);

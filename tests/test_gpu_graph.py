@@ -376,3 +376,34 @@ def test_all_zero_group_with_deferred_update_leaves_parameters_unchanged(cuda_li
         for a, b in zip(list(multi[gi].params) + list(multi[gi].momentum),
                         list(single[gi].params) + list(single[gi].momentum)):
             assert np.array_equal(to_host(a), to_host(b))
+
+
+def test_normuon_with_deferred_updates_overlap_on_and_off_bitwise(cuda_lib):
+    """dion3_step_normuon over three groups: with the overlap on, the two
+    groups before the last have their normalised updates (each row's lr times
+    its factor) carried by the last group's launches; with it off every group
+    scatters on its own.  Two steps give bit-identical selections, momenta,
+    parameters and second-moment states."""
+    f = 0.5
+    hp = d3.HParams(f=f, mu=0.95, lr=0.02)
+    nm = d3.NormuonParams()
+    runs = []
+    try:
+        for on in (True, False):
+            d3.set_overlap(on)
+            st = _build(f, seed=71)
+            v = [torch.zeros((b, n), dtype=torch.float32, device="cuda") for (n, m, b, _) in SHAPES]
+            ws = d3.alloc_workspace(d3.workspace_size(st[0], hp))
+            for _ in range(2):
+                d3.step_normuon(st[0], hp, nm, v, ws, sel_idx_out=st[3])
+            torch.cuda.synchronize()
+            d3.device_status()
+            runs.append((st, v))
+    finally:
+        d3.set_overlap(True)
+    (a, va), (b, vb) = runs
+    for gi in range(len(SHAPES)):
+        assert np.array_equal(a[3][gi].cpu().numpy(), b[3][gi].cpu().numpy())
+        for x, y in zip(a[1][gi] + a[2][gi], b[1][gi] + b[2][gi]):
+            assert np.array_equal(to_host(x), to_host(y))
+        assert torch.equal(va[gi], vb[gi])
