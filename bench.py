@@ -205,6 +205,50 @@ def job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def gemm_totals(trace: dict) -> dict:
+    """Launches, time and useful FLOPs of every GEMM entry of a launch trace
+    together (one entry per Newton-Schulz chain, or one per role with
+    DION3_TRACE_DETAIL)."""
+    return {k: sum(v[k] for v in trace.values() if v["useful_flops"] > 0)
+            for k in ("total_ms", "useful_flops", "launches")}
+
+
+def gemm_alone_and_overlap(trace: dict, steps: int, alone_trace: dict, alone_steps: int, peaks: dict):
+    """`roofline_alone` (the GEMM from the traced steps without the overlap)
+    and the `overlap` summary (None when the timed steps had no pooled work)."""
+    roof_alone = None
+    g_alone = gemm_totals(alone_trace)
+    if g_alone["total_ms"] > 0:
+        a_alone = g_alone["useful_flops"] / (g_alone["total_ms"] * 1e-3) / 1e12
+        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+        roof_alone = {"bound": "tensor", "kernel": "gemm_tcgen05", "achieved": a_alone, "peak": sus,
+                      "unit": "TFLOP/s", "frac": a_alone / sus, "peak_burst": peaks["bf16_tflops"],
+                      "frac_burst": a_alone / peaks["bf16_tflops"],
+                      "launches_per_step": g_alone["launches"] / alone_steps,
+                      "method": "3 extra traced steps with the accumulation overlap off"}
+        tr_alone = traffic_record("gemm_tcgen05")
+        roof_alone["traffic"] = tr_alone["dram_bytes_per_launch"] if tr_alone else None
+    overlap = None
+    if "accum_pool" in trace or "scatter_pool" in trace:
+        def per_step(tr, name, n):
+            return tr.get(name, {}).get("total_ms", 0.0) / n
+        overlap = {
+            "on": True,
+            "gemm_ms_per_step": gemm_totals(trace)["total_ms"] / steps,
+            "gemm_ms_per_step_alone": g_alone["total_ms"] / alone_steps,
+            "accum_standalone_ms_per_step": per_step(trace, "accum_rownorm", steps),
+            "accum_pool_rest_ms_per_step": per_step(trace, "accum_pool", steps),
+            "accum_ms_per_step_alone": per_step(alone_trace, "accum_rownorm", alone_steps),
+            "scatter_standalone_ms_per_step": per_step(trace, "scatter_update", steps),
+            "scatter_pool_rest_ms_per_step": per_step(trace, "scatter_pool", steps),
+            "scatter_ms_per_step_alone": per_step(alone_trace, "scatter_update", alone_steps),
+            "method": ("the first shape group's accumulation runs on its own; each later group's is a pool "
+                       "of rows taken by streaming warps inside the previous group's GEMM launches, the "
+                       "rest by a pool kernel; the last group's GEMM launches carry the scatter updates "
+                       "of up to two earlier groups the same way")}
+    return roof_alone, overlap
+
+
 def rank_barrier(world: int):
     if world > 1:
         import torch
@@ -613,37 +657,7 @@ def run_ours(args, rank, world, device_index):
     if graph is not None:
         step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
     paths = path_fractions(alone_trace, alone_steps, peaks)
-    roof_alone = None
-    # All GEMM entries together (one entry, or one per role with DION3_TRACE_DETAIL).
-    g_alone = {k: sum(v[k] for v in alone_trace.values() if v["useful_flops"] > 0)
-               for k in ("total_ms", "useful_flops", "launches")}
-    if g_alone["total_ms"] > 0:
-        a_alone = g_alone["useful_flops"] / (g_alone["total_ms"] * 1e-3) / 1e12
-        sus = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
-        roof_alone = {"bound": "tensor", "kernel": "gemm_tcgen05", "achieved": a_alone, "peak": sus,
-                      "unit": "TFLOP/s", "frac": a_alone / sus, "peak_burst": peaks["bf16_tflops"],
-                      "frac_burst": a_alone / peaks["bf16_tflops"],
-                      "launches_per_step": g_alone["launches"] / alone_steps,
-                      "method": "3 extra traced steps with the accumulation overlap off"}
-        tr_alone = traffic_record("gemm_tcgen05")
-        roof_alone["traffic"] = tr_alone["dram_bytes_per_launch"] if tr_alone else None
-    overlap = None
-    if "accum_pool" in trace:
-        gemm_ms = sum(v["total_ms"] for v in trace.values() if v["useful_flops"] > 0)
-        overlap = {
-            "on": True,
-            "gemm_ms_per_step": gemm_ms / args.steps,
-            "gemm_ms_per_step_alone": g_alone["total_ms"] / alone_steps,
-            "accum_standalone_ms_per_step": trace.get("accum_rownorm", {}).get("total_ms", 0.0) / args.steps,
-            "accum_pool_rest_ms_per_step": trace["accum_pool"]["total_ms"] / args.steps,
-            "accum_ms_per_step_alone": alone_trace.get("accum_rownorm", {}).get("total_ms", 0.0) / alone_steps,
-            "scatter_standalone_ms_per_step": trace.get("scatter_update", {}).get("total_ms", 0.0) / args.steps,
-            "scatter_pool_rest_ms_per_step": trace.get("scatter_pool", {}).get("total_ms", 0.0) / args.steps,
-            "scatter_ms_per_step_alone": alone_trace.get("scatter_update", {}).get("total_ms", 0.0) / alone_steps,
-            "method": ("the first shape group's accumulation runs on its own; each later group's is a pool "
-                       "of rows taken by streaming warps inside the previous group's GEMM launches, the "
-                       "rest by a pool kernel; the last group's GEMM launches carry the scatter updates "
-                       "of up to two earlier groups the same way")}
+    roof_alone, overlap = gemm_alone_and_overlap(trace, args.steps, alone_trace, alone_steps, peaks)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
