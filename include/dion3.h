@@ -312,7 +312,9 @@ dion3_status dion3_step(const dion3_group* groups, int32_t ngroups,
  * runs on its own, and each later group's is handed out row by row to
  * streaming warps inside the previous group's tensor-core GEMM launches, which
  * move it while the tensor cores work, with a memory-bound kernel finishing
- * the rows they did not reach.  Off, each group runs its steps in sequence,
+ * the rows they did not reach; the last group's launches carry the scatter
+ * updates (step c) of up to two groups before it the same way.  Off, each
+ * group runs its steps in sequence,
  * the groups on concurrent streams (see dion3_step).  Results are bit-identical
  * either way.  Process-wide; the environment variable DION3_OVERLAP=0 sets the
  * initial value to off.
