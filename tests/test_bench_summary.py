@@ -71,3 +71,21 @@ def test_no_overlap_summary_without_pooled_work():
     roof, ov = _bench().gemm_alone_and_overlap(trace, 2, alone, 3, PEAKS)
     assert ov is None
     assert roof is not None
+
+
+@pytest.mark.parametrize("per_role", [False, True])
+def test_path_fractions_split_gemm_and_memory_work(per_role):
+    """The Gram-NS path is every entry with useful FLOPs (its rate against the
+    sustained and burst tensor peaks), the select/update path every other
+    entry (its algorithmic bytes against the HBM copy bandwidth)."""
+    _, alone = _traces(per_role, pooled=False)
+    got = _bench().path_fractions(alone, 3, PEAKS)
+    tf = 12e12 / 26e-3 / 1e12
+    assert got["gram_ns_ms_per_step"] == pytest.approx(26.0 / 3)
+    assert got["gram_ns_tflops"] == pytest.approx(tf)
+    assert got["gram_ns_frac_sustained"] == pytest.approx(tf / 1600.0)
+    assert got["gram_ns_frac_burst"] == pytest.approx(tf / 2000.0)
+    gbs = (4.5e10 + 1.5e10) / 15e-3 / 1e9
+    assert got["select_update_ms_per_step"] == pytest.approx(5.0)
+    assert got["select_update_gbs"] == pytest.approx(gbs)
+    assert got["select_update_frac_hbm"] == pytest.approx(gbs / 7000.0)
