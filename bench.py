@@ -46,6 +46,7 @@ import hashlib
 import json
 import math
 import os
+import select
 import statistics
 import subprocess
 import sys
@@ -117,15 +118,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str):
+def traffic_record(kernel: str, workload: dict = None):
     """DRAM traffic per launch of `kernel` from a committed ncu summary, or None
-    if none exists or the kernel source changed since it was taken."""
+    if none exists, the kernel source changed since it was taken, or (when
+    `workload` is given) the record was taken on another workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         rec = json.load(fh).get(kernel)
     if not rec:
+        return None
+    if workload is not None and rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, rec["source"])
     with open(src, "rb") as fh:
@@ -148,6 +152,10 @@ class ClockSampler:
         self.gpu_index = gpu_index
 
     def start(self):
+        """Starts sampling and waits (at most 5 s) for the first sample, so the
+        sampler is running when the timed region begins; that first sample is
+        kept apart, as a fallback for regions shorter than the sampling period."""
+        self.first = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -155,20 +163,16 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+        if ready:
+            self.first = self.proc.stdout.readline()
 
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+    @staticmethod
+    def _summary(lines):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in (ln.split(",") for ln in lines if ln.strip()):
             try:
                 sm.append(float(r[1]))
                 mx.append(float(r[2]))
@@ -181,6 +185,23 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        got = self._summary(out.strip().splitlines())
+        if got is None and self.first:
+            got = self._summary([self.first])
+            if got is not None:
+                got["note"] = ("timed region shorter than the 100 ms sampling period: the sample taken "
+                               "just before it")
+        return got
 
 
 # ---------------------------------------------------------------------------
@@ -205,6 +226,12 @@ def job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def traffic_workload(args) -> dict:
+    """The key a traffic record is taken on: workload, f, operand type and
+    matrices per group (0: the whole set)."""
+    return {"workload": args.workload, "f": args.f, "ns_dtype": args.ns_dtype, "max_batch": args.max_batch}
+
+
 def gemm_totals(trace: dict) -> dict:
     """Launches, time and useful FLOPs of every GEMM entry of a launch trace
     together (one entry per Newton-Schulz chain, or one per role with
@@ -213,7 +240,8 @@ def gemm_totals(trace: dict) -> dict:
             for k in ("total_ms", "useful_flops", "launches")}
 
 
-def gemm_alone_and_overlap(trace: dict, steps: int, alone_trace: dict, alone_steps: int, peaks: dict):
+def gemm_alone_and_overlap(trace: dict, steps: int, alone_trace: dict, alone_steps: int, peaks: dict,
+                           workload: dict = None):
     """`roofline_alone` (the GEMM from the traced steps without the overlap)
     and the `overlap` summary (None when the timed steps had no pooled work)."""
     roof_alone = None
@@ -226,7 +254,7 @@ def gemm_alone_and_overlap(trace: dict, steps: int, alone_trace: dict, alone_ste
                       "frac_burst": a_alone / peaks["bf16_tflops"],
                       "launches_per_step": g_alone["launches"] / alone_steps,
                       "method": "3 extra traced steps with the accumulation overlap off"}
-        tr_alone = traffic_record("gemm_tcgen05")
+        tr_alone = traffic_record("gemm_tcgen05", workload)
         roof_alone["traffic"] = tr_alone["dram_bytes_per_launch"] if tr_alone else None
     overlap = None
     if "accum_pool" in trace or "scatter_pool" in trace:
@@ -622,7 +650,7 @@ def run_ours(args, rank, world, device_index):
         roof["frac_burst"] = achieved / peaks["bf16_tflops"]
     roof["kernel"] = dom_name
     roof["launches_per_step"] = dom["launches"] / args.steps
-    tr = traffic_record(dom_name)
+    tr = traffic_record(dom_name, traffic_workload(args))
     # The record is the GEMM on its own; launches that also carry accumulation
     # rows move more, so their traffic is left open.
     side = "accum_pool" in trace or "scatter_pool" in trace
@@ -657,7 +685,8 @@ def run_ours(args, rank, world, device_index):
     if graph is not None:
         step_roof["frac_graph"] = (t_tensor + t_hbm) / graph["ms_per_step"]
     paths = path_fractions(alone_trace, alone_steps, peaks)
-    roof_alone, overlap = gemm_alone_and_overlap(trace, args.steps, alone_trace, alone_steps, peaks)
+    roof_alone, overlap = gemm_alone_and_overlap(trace, args.steps, alone_trace, alone_steps, peaks,
+                                                 traffic_workload(args))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,

@@ -61,3 +61,18 @@ def test_bench_uses_the_record_only_for_the_same_source():
         assert got is not None and got["dram_bytes_per_launch"] > 0
     else:
         assert got is None
+
+
+def test_record_is_used_only_for_its_own_workload():
+    """The record names the workload its captures were taken on; bench.py
+    attaches it to that workload's line only (another workload, f, operand
+    type or a capped batch gets no traffic figure)."""
+    rec = _record()
+    wl = rec["workload"]
+    bench = _bench()
+    with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
+        same = hashlib.sha256(fh.read()).hexdigest() == rec["source_sha256"]
+    if same:
+        assert bench.traffic_record("gemm_tcgen05", dict(wl)) is not None
+    for key, other in (("workload", "gapped"), ("f", 0.125), ("ns_dtype", "bf16"), ("max_batch", 4)):
+        assert bench.traffic_record("gemm_tcgen05", dict(wl, **{key: other})) is None
