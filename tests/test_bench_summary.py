@@ -89,3 +89,16 @@ def test_path_fractions_split_gemm_and_memory_work(per_role):
     assert got["select_update_ms_per_step"] == pytest.approx(5.0)
     assert got["select_update_gbs"] == pytest.approx(gbs)
     assert got["select_update_frac_hbm"] == pytest.approx(gbs / 7000.0)
+
+
+def test_clock_summary_parses_nvidia_smi_rows():
+    """Median SM clock, maximum clock and the throttle reasons seen active, from
+    the CSV rows the sampler reads (index, sm, max sm, power, reasons active,
+    hw_slowdown, hw_thermal, sw_thermal, sw_power_cap)."""
+    rows = ["0, 1500, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1600, 2070, 1395.1, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbled"]
+    got = _bench().ClockSampler._summary(rows)
+    assert got == {"sm_mhz": 1600.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert _bench().ClockSampler._summary(["", "garbled"]) is None
